@@ -1,0 +1,205 @@
+/*
+ * attn.h - C ABI of libattn.so: exact softmax attention computed blockwise over
+ * KV tiles and chunks, with the running (m, l, O) triplet merged by online
+ * softmax, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, by page title and section:
+ *   [PREFILL]  "kernbench2 _gqa_prefill_long.py" - gqa_prefill_long_kernel:
+ *              step 0 partial (scores = Q.K^T, m = rowmax, exp(scores - m),
+ *              l = rowsum, O = exp_scores . V), ring steps 1..C-1 (KV block
+ *              rotation and the online-softmax merge), final normalise O / l.
+ *   [DECODE]   "kernbench2 _attention_mesh_mlo.py" - one-shot local partial of
+ *              a sequence-sharded KV, the (m, l, o) merge, final O := o / l.
+ *   [BOUNDS]   "[pallas] Support dependent Tile.end bounds in Pallas" - inner KV
+ *              loop over [kv_begin, min(kv_end, tile_q.end)), trip count
+ *              cdiv(active_end - begin, block_k), tail mask, flattened jagged
+ *              worklists, jagged KV end seq_offsets[seq_idx + 1].
+ *
+ * Conventions for every call
+ *   Layouts are token-major and dense (no strides):
+ *     Q, O            [B, S_q, h_q, D]      K, V  [B, S_kv, h_kv, D]
+ *     LSE, m, l       [B, h_q, S_q]  fp32   unnormalised O  [B, S_q, h_q, D] fp32
+ *     jagged Q/K/V/O  [total_tokens, H, D]  jagged LSE      [H, total_tokens]
+ *   Query head h reads KV head h / (h_q / h_kv) (contiguous groups).
+ *   Scores are s = scale * q.k; LSE = ln sum_j exp(s_j) (natural log).
+ *   Causal masking: key j is visible to query i iff pos(j) <= pos(i), with
+ *   query and key positions in one index space (top-left alignment).
+ *   A row that sees no key yields O = 0 and LSE = -inf; its partial triplet is
+ *   the merge identity (m, l, O) = (-inf, 0, 0).
+ *   Inputs are fp16 or bf16 (all of Q, K, V the same); accumulation is fp32;
+ *   P is rounded to the input type before P.V; outputs O are rounded to the
+ *   input type (nearest even).
+ *
+ *   Ownership: the caller owns every buffer and the stream; the library never
+ *   allocates device memory.  Scratch space comes from the caller through a
+ *   `workspace` argument sized by the matching *_workspace_bytes() helper.
+ *   Every call is asynchronous on `stream` (0 = legacy default stream).
+ *   Device pointers must be 16-byte aligned (LSE, m, l: 4-byte aligned).
+ *
+ *   Errors: every call returns an attn_status_t and never aborts.  Invalid
+ *   arguments are rejected on the host before any launch.  Conditions only the
+ *   device can see (a barrier wait that gave up, malformed seq_offsets) are
+ *   recorded in a per-library device status word and reported, then cleared,
+ *   by attn_last_device_status().
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* same object as cudaStream_t */
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment, h_q % h_kv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement (e.g. D) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, tensor map) */
+  ATTN_ERR_TIMEOUT = 4,     /* a device-side wait gave up (reported by attn_last_device_status) */
+  ATTN_ERR_DEVICE_INPUT = 5 /* device-side input check failed, e.g. non-monotone seq_offsets */
+} attn_status_t;
+
+typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/* Tile sizes of the prefill kernels: BLOCK_M query rows x BLOCK_N keys. */
+#define ATTN_BLOCK_M 128
+#define ATTN_BLOCK_N 128
+
+/*
+ * attn_prefill - causal or full prefill attention with a ring-order chunk walk.
+ *   [PREFILL] (Algorithm paragraph of the kernel docstring; P6b ring rotation)
+ *   [BOUNDS]  (dependent inner-loop end, trip count, tail mask)
+ *
+ * The KV sequence is cut into num_chunks chunks of ceil(S_kv / num_chunks) keys.
+ * Each Q tile of ATTN_BLOCK_M rows visits the chunks in ring order (c0 + t) mod C,
+ * starting at the chunk c0 = min(C-1, q_tile_start / chunk_len) that holds its
+ * first position; the running (m, l, O) carries across chunks (the page's merge).
+ * With causal = 1 a chunk whose first key lies after the tile's last query is
+ * skipped, and inside a chunk only cdiv(min(chunk_end, q_tile_end) - chunk_start,
+ * ATTN_BLOCK_N) KV tiles are visited (fully masked tiles are pruned, not masked).
+ *
+ *   q [B,S_q,h_q,D], k/v [B,S_kv,h_kv,D], o [B,S_q,h_q,D] (input dtype),
+ *   lse [B,h_q,S_q] fp32 or NULL.  D in {64, 128, 256}.  num_chunks >= 1.
+ *   S_q = 0 or B = 0 is a no-op; S_kv = 0 writes O = 0 and LSE = -inf.
+ */
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
+                           int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale, int causal,
+                           int num_chunks, attn_stream_t stream);
+
+/*
+ * attn_partial - the partial triplet of one KV range (one ring step's partial).
+ *   [PREFILL] (step 0 partial / per-step partial on the rotated KV block)
+ *
+ * Keys k[:, kv_begin:kv_end] sit at positions kv_begin..kv_end-1 (k's own index
+ * space); query i sits at position q_pos0 + i.  Writes, per query row,
+ *   m = max_j s_ij, l = sum_j exp(s_ij - m), o_unnorm = sum_j exp(s_ij - m) v_j
+ * over the visible keys of the range (the identity (-inf, 0, 0) if none).
+ *   m, l [B,h_q,S_q] fp32; o_unnorm [B,S_q,h_q,D] fp32.
+ *   0 <= kv_begin <= kv_end <= S_kv.  To fill stacked partials [C, ...] pass
+ *   pointers offset by c * (one partial's element count).
+ */
+attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o_unnorm,
+                           int B, int S_q, int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale,
+                           int causal, int q_pos0, int kv_begin, int kv_end, attn_stream_t stream);
+
+/*
+ * attn_merge - fold C partial triplets per row and normalise.
+ *   [PREFILL] (online-softmax merge into the running (m, l, O); final normalise)
+ *   [DECODE]  (merge-from-W / merge-from-E; final normalize O := o / l)
+ *
+ * Per row: M = max_c m_c; l = sum_c l_c exp(m_c - M); O = sum_c o_c exp(m_c - M) / l;
+ * LSE = M + ln l.  Partials with m_c = -inf contribute nothing; a row whose
+ * partials are all empty gives O = 0, LSE = -inf.
+ *   m, l [C,B,H,S_q] fp32; o_unnorm [C,B,S_q,H,D] fp32;
+ *   out [B,S_q,H,D] in out_dtype; lse [B,H,S_q] fp32 or NULL.  D in {64,128,256}.
+ */
+attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, int C, int B, int S_q, int H,
+                         int D, void* out, attn_dtype_t out_dtype, float* lse, attn_stream_t stream);
+
+/*
+ * attn_jagged - variable-length causal (or full) self-attention over packed
+ * sequences.
+ *   [BOUNDS] (jagged KV end seq_offsets[seq_idx + 1]; flattened worklists with
+ *            compute_end = min(source_end, compact_end) driving the trip count)
+ *
+ * Sequence b spans tokens [seq_offsets[b], seq_offsets[b+1]) and attends only to
+ * itself.  Q tiles start at the sequence start.  A device kernel first builds the
+ * flattened worklist (one item per (sequence, Q tile)) from the device-resident
+ * seq_offsets into `workspace`; the attention kernel then runs one CTA per
+ * (item, head).  No host synchronisation is needed.
+ *   q/k/v/o [total_tokens,H,D]; lse [H,total_tokens] fp32 or NULL;
+ *   seq_offsets int32 [num_seqs+1], device memory, non-decreasing, from 0 to at
+ *   most total_tokens, every length <= max_seqlen (violations are reported as
+ *   ATTN_ERR_DEVICE_INPUT by attn_last_device_status and their tokens are not
+ *   written).  workspace >= attn_jagged_workspace_bytes(num_seqs, total_tokens,
+ *   max_seqlen) bytes, 16-byte aligned.
+ */
+attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* seq_offsets, int num_seqs, int total_tokens, int max_seqlen, int H, int D,
+                          attn_dtype_t dtype, float scale, int causal, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream);
+size_t attn_jagged_workspace_bytes(int num_seqs, int total_tokens, int max_seqlen);
+
+/*
+ * attn_decode_splitkv - one query per sequence against a long KV, split-KV.
+ *   [DECODE] (KV sequence-sharded and read in place; one-shot local partial per
+ *            shard; triplets merged; final normalize)
+ *
+ * The KV sequence is cut into num_splits chunks of ceil(S_kv / num_splits) keys
+ * (trailing chunks may be empty: identity triplets).  One kernel computes a
+ * partial (m, l, o) per (batch, query head, chunk) into `workspace`, a second
+ * kernel merges them (as attn_merge).  Workspace layout (fp32, contiguous):
+ *   m [num_splits,B,h_q], l [num_splits,B,h_q], o [num_splits,B,h_q,D].
+ *   q [B,h_q,D]; k/v [B,S_kv,h_kv,D]; o [B,h_q,D]; lse [B,h_q] fp32 or NULL.
+ *   D in {64,128,256}; h_q / h_kv <= 16.
+ */
+attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                  int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+size_t attn_decode_workspace_bytes(int B, int h_q, int D, int num_splits);
+
+/*
+ * attn_last_device_status - synchronise `stream`, then return and clear the
+ * device-side status (ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_INPUT) raised by any
+ * kernel of the library since the previous call; ATTN_OK if none.
+ */
+attn_status_t attn_last_device_status(attn_stream_t stream);
+
+/*
+ * attn_selftest_wait_timeout - failure-detection self-test.  Launches one thread
+ * that waits on a shared-memory barrier nothing ever completes, through the same
+ * bounded wait every kernel of the library uses, limited to timeout_ns
+ * (1 ms .. 10 s).  The wait gives up, records ATTN_ERR_TIMEOUT in the device
+ * status and the kernel returns normally, leaving the context usable; the
+ * caller reads the status with attn_last_device_status().  Has no counterpart
+ * on the pages: it tests this library's own wait discipline.
+ */
+attn_status_t attn_selftest_wait_timeout(uint64_t timeout_ns, attn_stream_t stream);
+
+/* Static description of a status code; never NULL. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_tile_walk - host-side enumeration of the KV tiles one Q tile visits, by
+ * the same scheduling code the kernels run (for tests and tooling).
+ *   [BOUNDS] (dependent end, trip count); [PREFILL] (ring order, P6b)
+ *
+ * Q rows [q_lo, q_hi) at positions q_pos0 + i; keys [kv_lo, kv_hi) at positions
+ * kv_pos0 + j, cut into num_chunks ring chunks.  Writes up to max_tiles entries
+ * (chunk, tile_start, mask_end) in visiting order, where mask_end is the first
+ * key index that the tile's tail mask excludes, and stores the full count in
+ * *n_tiles.  Returns ATTN_ERR_INVALID_ARG on bad sizes or null pointers.
+ */
+attn_status_t attn_tile_walk(int q_lo, int q_hi, int kv_lo, int kv_hi, int block_n, int causal, int num_chunks,
+                             int q_pos0, int kv_pos0, int* chunk, int* tile_start, int* mask_end, int max_tiles,
+                             int* n_tiles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

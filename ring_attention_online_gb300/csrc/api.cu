@@ -1,0 +1,293 @@
+// C ABI of libattn.so: argument validation, tensor-map encoding and launches.
+// Every public function checks its arguments on the host and returns a status
+// before anything reaches the device; nothing here allocates device memory.
+#include <math.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "schedule.cuh"
+
+namespace attn {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a dense [B, S, H, D] tensor of 16-bit elements, read as boxes
+// of `box_rows` tokens x 64 columns (128 bytes, 128-byte swizzle) of one head.
+bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int H, long long S, int B, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(S > 0 ? S : 1), (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)(S > 0 ? S : 1) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+             const_cast<void*>(ptr), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
+bool dtype_ok(attn_dtype_t d) { return d == ATTN_FP16 || d == ATTN_BF16; }
+bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
+constexpr float kLog2e = 1.4426950408889634f;
+
+attn_status_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                             const CUtensorMap& mv, int mode, bool bf16, int D, dim3 grid, cudaStream_t s) {
+  switch (D) {
+    case 64: return launch_prefill_d64(p, mq, mk, mv, mode, bf16, grid, s);
+    case 128: return launch_prefill_d128(p, mq, mk, mv, mode, bf16, grid, s);
+    case 256: return launch_prefill_d256(p, mq, mk, mv, mode, bf16, grid, s);
+  }
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+// Shared checks of the dense prefill-shaped calls.
+attn_status_t check_dense(const void* q, const void* k, const void* v, int B, int S_q, int S_kv, int h_q, int h_kv,
+                          int D, attn_dtype_t dtype, float scale, int causal) {
+  if (!q || !k || !v) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || S_q < 0 || S_kv < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype) || !scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return ATTN_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)S_q > 0x7fffff80LL || (long long)S_kv > 0x7fffff80LL) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B > 65535 || (long long)h_q > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+size_t jagged_max_items(int num_seqs, int total_tokens) {
+  // sum_b ceil(L_b / BM) <= (T + num_seqs * (BM - 1)) / BM
+  return ((size_t)total_tokens + (size_t)num_seqs * (ATTN_BLOCK_M - 1)) / ATTN_BLOCK_M;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
+                           int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale, int causal,
+                           int num_chunks, attn_stream_t stream) {
+  attn_status_t st = check_dense(q, k, v, B, S_q, S_kv, h_q, h_kv, D, dtype, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4)) || num_chunks < 1) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S_q == 0) return ATTN_OK;
+  const bool bf16 = dtype == ATTN_BF16;
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.h_q = h_q;
+  p.h_kv = h_kv;
+  p.group = h_q / h_kv;
+  p.causal = causal;
+  p.num_chunks = num_chunks;
+  p.q_pos0 = 0;
+  p.kv_pos0 = 0;
+  p.kv_lo = 0;
+  p.kv_hi = S_kv;
+  p.scale_log2 = scale * kLog2e;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
+      !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
+    return ATTN_ERR_CUDA;
+  const dim3 grid((S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, h_q, B);
+  return launch_prefill(p, mq, mk, mv, kModeDense, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o_unnorm,
+                           int B, int S_q, int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale,
+                           int causal, int q_pos0, int kv_begin, int kv_end, attn_stream_t stream) {
+  attn_status_t st = check_dense(q, k, v, B, S_q, S_kv, h_q, h_kv, D, dtype, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (!m || !l || !o_unnorm || !aligned(m, 4) || !aligned(l, 4) || !aligned(o_unnorm, 16)) return ATTN_ERR_INVALID_ARG;
+  if (kv_begin < 0 || kv_end < kv_begin || kv_end > S_kv) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S_q == 0) return ATTN_OK;
+  const bool bf16 = dtype == ATTN_BF16;
+  PrefillParams p{};
+  p.m_out = m;
+  p.l_out = l;
+  p.o_part = o_unnorm;
+  p.B = B;
+  p.S_q = S_q;
+  p.S_kv = S_kv;
+  p.h_q = h_q;
+  p.h_kv = h_kv;
+  p.group = h_q / h_kv;
+  p.causal = causal;
+  p.num_chunks = 1;
+  p.q_pos0 = q_pos0;
+  p.kv_pos0 = 0;
+  p.kv_lo = kv_begin;
+  p.kv_hi = kv_end;
+  p.scale_log2 = scale * kLog2e;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
+      !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
+    return ATTN_ERR_CUDA;
+  const dim3 grid((S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, h_q, B);
+  return launch_prefill(p, mq, mk, mv, kModePartial, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, int C, int B, int S_q, int H, int D,
+                         void* out, attn_dtype_t out_dtype, float* lse, attn_stream_t stream) {
+  if (!m || !l || !o_unnorm || !out) return ATTN_ERR_INVALID_ARG;
+  if (C < 1 || B < 0 || S_q < 0 || H < 1) return ATTN_ERR_INVALID_ARG;
+  if (!dtype_ok(out_dtype)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(m, 4) || !aligned(l, 4) || !aligned(o_unnorm, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || S_q == 0) return ATTN_OK;
+  return launch_merge(m, l, o_unnorm, C, B, S_q, H, D, out, out_dtype == ATTN_BF16, lse,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_jagged_workspace_bytes(int num_seqs, int total_tokens, int max_seqlen) {
+  (void)max_seqlen;
+  if (num_seqs < 0 || total_tokens < 0) return 0;
+  return 16 + 16 * jagged_max_items(num_seqs, total_tokens);
+}
+
+attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* seq_offsets, int num_seqs, int total_tokens, int max_seqlen, int H, int D,
+                          attn_dtype_t dtype, float scale, int causal, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream) {
+  attn_status_t st = check_dense(q, k, v, 1, total_tokens, total_tokens, H, H, D, dtype, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (!o || !seq_offsets || !aligned(o, 16) || (lse && !aligned(lse, 4)) || !aligned(seq_offsets, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (num_seqs < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_tokens == 0) return ATTN_OK;
+  if (!workspace || !aligned(workspace, 16) || workspace_bytes < attn_jagged_workspace_bytes(num_seqs, total_tokens, max_seqlen))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t max_items = jagged_max_items(num_seqs, total_tokens);
+  if (max_items > 0x7fffffffULL || H > 65535) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* wl = static_cast<int*>(workspace);
+  st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, ATTN_BLOCK_M, wl, (int)max_items, s);
+  if (st != ATTN_OK) return st;
+  const bool bf16 = dtype == ATTN_BF16;
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = 1;
+  p.S_q = total_tokens;
+  p.S_kv = total_tokens;
+  p.h_q = H;
+  p.h_kv = H;
+  p.group = 1;
+  p.causal = causal;
+  p.num_chunks = 1;
+  p.scale_log2 = scale * kLog2e;
+  p.work_count = wl;
+  p.work_items = reinterpret_cast<const int4*>(wl + 4);
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, bf16, D, H, total_tokens, 1, ATTN_BLOCK_M) ||
+      !make_map(&mk, k, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N) ||
+      !make_map(&mv, v, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N))
+    return ATTN_ERR_CUDA;
+  const dim3 grid((unsigned)max_items, H, 1);
+  return launch_prefill(p, mq, mk, mv, kModeJagged, bf16, D, grid, s);
+}
+
+size_t attn_decode_workspace_bytes(int B, int h_q, int D, int num_splits) {
+  if (B < 0 || h_q < 0 || D < 0 || num_splits < 0) return 0;
+  const size_t rows = (size_t)num_splits * B * h_q;
+  const size_t ml = (rows * 2 * sizeof(float) + 15) & ~size_t(15);
+  return ml + rows * D * sizeof(float);
+}
+
+attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                  int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  attn_status_t st = check_dense(q, k, v, B, 1, S_kv, h_q, h_kv, D, dtype, scale, 0);
+  if (st != ATTN_OK) return st;
+  if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4)) || num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if (h_q / h_kv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0) return ATTN_OK;
+  if (num_splits > 65535 || h_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 16) || workspace_bytes < attn_decode_workspace_bytes(B, h_q, D, num_splits))
+    return ATTN_ERR_INVALID_ARG;
+  const bool bf16 = dtype == ATTN_BF16;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)num_splits * B * h_q;
+  float* wm = static_cast<float*>(workspace);
+  float* wl = wm + rows;
+  float* wo = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * 2 * sizeof(float) + 15) & ~size_t(15)));
+  CUtensorMap mk, mv;
+  if (!make_map(&mk, k, bf16, D, h_kv, S_kv, B, 64) || !make_map(&mv, v, bf16, D, h_kv, S_kv, B, 64))
+    return ATTN_ERR_CUDA;
+  st = launch_decode_partial(q, mk, mv, wm, wl, wo, B, S_kv, h_q, h_kv, D, bf16, scale * kLog2e, num_splits, s);
+  if (st != ATTN_OK) return st;
+  return launch_merge(wm, wl, wo, num_splits, B, 1, h_q, D, o, bf16, lse, s);
+}
+
+attn_status_t attn_last_device_status(attn_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned int v = prefill_d64_take_status(s) | prefill_d128_take_status(s) | prefill_d256_take_status(s) |
+                         worklist_take_status(s) | decode_take_status(s);
+  if (v & kStatusTimeout) return ATTN_ERR_TIMEOUT;
+  if (v & kStatusDeviceInput) return ATTN_ERR_DEVICE_INPUT;
+  return ATTN_OK;
+}
+
+attn_status_t attn_selftest_wait_timeout(uint64_t timeout_ns, attn_stream_t stream) {
+  if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+  return launch_selftest_timeout(timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_DEVICE_INPUT: return "device-side input check failed";
+  }
+  return "unknown status";
+}
+
+attn_status_t attn_tile_walk(int q_lo, int q_hi, int kv_lo, int kv_hi, int block_n, int causal, int num_chunks,
+                             int q_pos0, int kv_pos0, int* chunk, int* tile_start, int* mask_end, int max_tiles,
+                             int* n_tiles) {
+  if (!n_tiles || block_n < 1 || num_chunks < 1 || q_hi < q_lo || kv_hi < kv_lo || max_tiles < 0 ||
+      (max_tiles > 0 && (!chunk || !tile_start || !mask_end)) || (causal != 0 && causal != 1))
+    return ATTN_ERR_INVALID_ARG;
+  TileWalk w;
+  w.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, causal, num_chunks, block_n);
+  const int total = w.count();
+  int i = 0, c, st, me;
+  while (i < max_tiles && w.next(c, st, me)) {
+    chunk[i] = c;
+    tile_start[i] = st;
+    mask_end[i] = me;
+    ++i;
+  }
+  *n_tiles = total;
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,513 @@
+// Blockwise online-softmax attention forward, tcgen05 + TMA, one Q tile of
+// 128 rows per CTA.
+//
+// What it computes, by source:
+//  * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel: per KV block,
+//    scores = Q.K^T, m = rowmax, exp(scores - m), l = rowsum, O = exp . V; each
+//    block merged into the running (m, l, O) with m_new = max(m, m_step) and the
+//    factors exp(m - m_new), exp(m_step - m_new); at the end O / l.  Here the
+//    "blocks" are 128-key tiles and the running triplet lives in registers (m, l)
+//    and TMEM (O); the page's ring steps become a ring-order walk over chunks.
+//  * "[pallas] Support dependent Tile.end bounds in Pallas": the tile walk ends
+//    at min(kv_end, tile_q.end) (no fully masked tile is visited); only the
+//    diagonal and tail tiles are masked.
+//
+// CTA layout (192 threads):
+//   warp 0      TMA producer: Q tile once, then K/V 128-column slabs through a
+//               ring of NST shared-memory stages, in the order the MMA needs.
+//   warp 1      TMEM owner and single-thread tcgen05 issuer:
+//               S(0), then per tile j: S(j+1), PV(j).  S(j) = Q.K_j^T goes to one
+//               of two 128-column TMEM buffers; PV(j) reads P(j) (bf16/fp16,
+//               written over S(j) by the softmax warps) as the TMEM A operand.
+//   warps 2..5  softmax + epilogue, one query row per thread (TMEM lane).
+//               Scores are scaled into the exp2 domain; the running max is
+//               raised lazily (only when it grows by more than 2^8), so O is
+//               rescaled in TMEM only on those tiles - the result is the same
+//               up to rounding because l and O always share one reference max.
+//
+// Every wait is bounded (see mbar_wait_bounded); a timeout sets the library's
+// device status, the CTA skips its remaining work, drains its copies and MMAs
+// and frees TMEM before returning.
+#pragma once
+
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "schedule.cuh"
+
+namespace attn {
+
+static __device__ unsigned int g_prefill_status;
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int SC = D < 128 ? D : 128;  // columns per K/V slab (one smem stage)
+  static constexpr int NH = D / SC;             // slabs per K or V tile
+  static constexpr int BLK_PER_SLAB = SC / 64;  // 64-column TMA blocks per slab
+  static constexpr int BLOCK_BYTES = 128 * 128; // one TMA block: 128 rows x 128 bytes
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int SLAB_BYTES = BN * SC * 2;
+  static constexpr int DATA_BUDGET = 224 * 1024;
+  static constexpr int NST = (DATA_BUDGET - Q_BYTES) / SLAB_BYTES;
+  static constexpr int SMEM_BYTES = Q_BYTES + NST * SLAB_BYTES + 1024;  // + 1 KB alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  // S(j) / P(j) live in TMEM columns [128*(j%2), 128*(j%2)+128); O after them
+  static constexpr uint32_t O_COL = 256;
+  static constexpr int THREADS = 192;
+  static_assert(D == 64 || D == 128 || D == 256, "head dim");
+  static_assert(NST >= 2, "at least two K/V stages");
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// Bounded wait used by every role; also gives up as soon as another CTA of
+// any launch has reported a timeout (so a broken pipeline ends quickly).
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort, uint32_t site) {
+  if (mbar_try_wait(smem_u32(bar), parity)) return true;
+  if (*reinterpret_cast<volatile unsigned int*>(&g_prefill_status) & kStatusTimeout) {
+    *abort = 1u;
+    return false;
+  }
+  return mbar_wait_bounded(bar, parity, abort, &g_prefill_status, kStatusTimeout | (site << kStatusSiteShift),
+                           kWaitTimeoutNs);
+}
+
+// Wait used only while tearing down after an abort: ignores the abort flag.
+__device__ __forceinline__ void pf_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      atomicOr(&g_prefill_status, kStatusTimeout | (0x80u << kStatusSiteShift));
+      return;
+    }
+  }
+}
+
+template <int D, bool kBf16, int kMode>
+__global__ void __launch_bounds__(192, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
+  using C = PrefillCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_o, bar_fin;
+  __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
+  __shared__ uint64_t bar_s[2], bar_p[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t abort_flag;
+
+  // ------------------------------------------------------------ work item
+  int b, h, q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0;
+  if constexpr (kMode == kModeJagged) {
+    const int item = blockIdx.x;
+    if (item >= *p.work_count) return;  // the grid is an upper bound on the item count
+    const int4 it = p.work_items[item];
+    b = 0;
+    h = blockIdx.y;
+    q_lo = it.z;
+    q_hi = it.z + it.w;
+    kv_lo = it.x;
+    kv_hi = it.x + it.y;  // seq_offsets[seq_idx + 1]
+    q_pos0 = 0;
+    kv_pos0 = 0;
+  } else {
+    // causal: longest Q tiles first, so the short ones fill the tail
+    const int qt = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    b = blockIdx.z;
+    h = blockIdx.y;
+    q_lo = qt * C::BM;
+    q_hi = min(q_lo + C::BM, p.S_q);
+    kv_lo = p.kv_lo;
+    kv_hi = p.kv_hi;
+    q_pos0 = p.q_pos0;
+    kv_pos0 = p.kv_pos0;
+  }
+  const int hk = h / p.group;
+  TileWalk walk;
+  walk.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, p.num_chunks, C::BN);
+  const int n = walk.count();
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::Q_BYTES;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_o, 1);
+    mbar_init(&bar_fin, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_p[i], 128);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ========================================================== TMA producer
+    if (lane == 0 && n > 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
+      for (int blk = 0; blk < D / 64; ++blk) tma_load_4d(sQ + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, h, q_lo, b);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      auto push = [&](const CUtensorMap* map, int start) -> bool {
+        for (int hs = 0; hs < C::NH; ++hs) {
+          if (!pf_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
+          uint8_t* dst = sKV + stage * C::SLAB_BYTES;
+          mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
+          for (int blk = 0; blk < C::BLK_PER_SLAB; ++blk)
+            tma_load_4d(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], hs * C::SC + blk * 64, hk, start, b);
+          ++issued;
+          if (++stage == C::NST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        return true;
+      };
+      TileWalk kw = walk, vw = walk;
+      int ch, st, me;
+      kw.next(ch, st, me);
+      ok = push(&mk, st);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          kw.next(ch, st, me);
+          ok = push(&mk, st);
+          if (!ok) break;
+        }
+        vw.next(ch, st, me);
+        ok = push(&mv, st);
+      }
+      if (abort_flag) {
+        // copies may still be landing in shared memory: wait for them
+        pf_drain(&bar_q, 0);
+        const int outstanding = issued < C::NST ? issued : C::NST;
+        for (int i = 0; i < outstanding; ++i) {
+          const int pos = issued - 1 - i;
+          pf_drain(&bar_full[pos % C::NST], (uint32_t)((pos / C::NST) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ========================================================== MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
+      constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, C::SC, kBf16, true);
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t skv = smem_u32(sKV);
+      int stage = 0;
+      uint32_t phase = 0;
+      auto advance = [&]() {
+        if (++stage == C::NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      };
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+        for (int hs = 0; hs < C::NH; ++hs) {
+          if (!pf_wait(&bar_full[stage], phase, &abort_flag, 2)) return false;
+          tc_fence_after_sync();
+          const uint32_t kbase = skv + stage * C::SLAB_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < C::SC / 16; ++ks) {
+            const uint32_t qoff = (hs * C::BLK_PER_SLAB + ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+            const uint32_t koff = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+            mma_ss(d_tmem, smem_desc_sw128(sq + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024), kIdescS,
+                   (hs | ks) != 0);
+          }
+          mma_commit(&bar_empty[stage]);
+          advance();
+        }
+        mma_commit(&bar_s[j & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        if (!pf_wait(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3)) return false;
+        tc_fence_after_sync();
+        const uint32_t p_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+        for (int hs = 0; hs < C::NH; ++hs) {
+          if (!pf_wait(&bar_full[stage], phase, &abort_flag, 4)) return false;
+          tc_fence_after_sync();
+          const uint32_t vbase = skv + stage * C::SLAB_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < C::BN / 16; ++ks)
+            mma_ts(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, smem_desc_sw128(vbase + ks * 2048, 16384, 1024),
+                   kIdescPV, (j > 0 || ks > 0));
+          mma_commit(&bar_empty[stage]);
+          advance();
+        }
+        mma_commit(&bar_o);
+        return true;
+      };
+      bool ok = pf_wait(&bar_q, 0, &abort_flag, 5);
+      tc_fence_after_sync();
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          ok = issue_s(j + 1);
+          if (!ok) break;
+        }
+        ok = issue_pv(j);
+      }
+      // every MMA issued above must finish before TMEM is released
+      mma_commit(&bar_fin);
+      pf_drain(&bar_fin, 0);
+    }
+  } else {
+    // ========================================================== softmax + epilogue
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const int q_row = q_lo + row;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const float c = p.scale_log2;  // > 0
+    float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
+    float l_run = 0.f;             // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
+    float lr_run = 0.f;            // sum of the rounded P the MMA multiplies V by: normalises O
+    float m_max = -CUDART_INF_F;   // true running max (partial mode)
+    bool ok = true;
+    TileWalk sw = walk;
+    for (int j = 0; j < n; ++j) {
+      int ch, kstart, mend;
+      sw.next(ch, kstart, mend);
+      const int buf = j & 1;
+      if (!pf_wait(&bar_s[buf], (uint32_t)((j >> 1) & 1), &abort_flag, 6)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t scol = lane_addr + static_cast<uint32_t>(buf * 128);
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(scol, r0);
+      tmem_ld32(scol + 32, r1);
+      tmem_ld32(scol + 64, r2);
+      tmem_ld32(scol + 96, r3);
+      tmem_ld_wait(r0);
+      tmem_ld_wait(r1);
+      tmem_ld_wait(r2);
+      tmem_ld_wait(r3);
+
+      // mask the diagonal / tail tile: key kstart+i is visible iff i < lim
+      const bool need_mask =
+          (kstart + C::BN > mend) ||
+          (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo));
+      if (need_mask) {
+        int lim = mend - kstart;
+        if (p.causal) {
+          const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
+          lim = (int)(lc < lim ? lc : lim);
+        }
+        const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= lim) r0[i] = ninf;
+          if (i + 32 >= lim) r1[i] = ninf;
+          if (i + 64 >= lim) r2[i] = ninf;
+          if (i + 96 >= lim) r3[i] = ninf;
+        }
+      }
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r1[i])),
+                             fmaxf(__uint_as_float(r2[i]), __uint_as_float(r3[i]))));
+      }
+      const float m_tile = mx * c;  // -inf when the whole row is masked
+      if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
+      const float m_new = fmaxf(m_run, m_tile);
+      const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
+      float alpha = 1.f;
+      if (raise) {
+        alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
+        m_run = m_new;
+        l_run *= alpha;
+        lr_run *= alpha;
+      }
+      const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+      float sum = 0.f, sum_r = 0.f;
+      uint32_t pk[16];
+      auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), c, neg_m));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), c, neg_m));
+          pk[i] = pack_half2<kBf16>(p0, p1);
+          sum += p0 + p1;
+          // O is normalised by the sum of the rounded weights it was built
+          // from, so O / l is a weighted mean with consistent weights
+          const float2 pr = unpack_half2<kBf16>(pk[i]);
+          sum_r += pr.x + pr.y;
+        }
+        tmem_st16(scol + col, pk);
+      };
+      // P(j) overwrites the first 64 columns of S(j), already in registers
+      pack_chunk(r0, 0);
+      pack_chunk(r1, 16);
+      pack_chunk(r2, 32);
+      pack_chunk(r3, 48);
+      l_run += sum;
+      lr_run += sum_r;
+
+      if (j > 0) {
+        // PV(j-1) must be complete before O is rescaled (and it keeps the
+        // phase bookkeeping of bar_o exact)
+        if (!pf_wait(&bar_o, (uint32_t)((j - 1) & 1), &abort_flag, 7)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + C::O_COL + cc * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(lane_addr + C::O_COL + cc * 32, o);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bar_p[buf]);
+    }
+    if (ok && n > 0) {
+      ok = pf_wait(&bar_o, (uint32_t)((n - 1) & 1), &abort_flag, 8);
+      tc_fence_after_sync();
+    }
+    if (ok) {
+      const bool row_valid = q_row < q_hi;
+      const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
+      const size_t lse_idx = ((size_t)b * p.h_q + h) * p.S_q + q_row;
+      constexpr float kLn2 = 0.693147180559945309f;
+      if constexpr (kMode != kModePartial) {
+        const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(lane_addr + C::O_COL + cc * 32, o);
+            tmem_ld_wait(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
+        }
+        if (p.lse != nullptr && row_valid)
+          p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
+      } else {
+        const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
+        const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
+        // O re-weighted so that O / l equals the consistently normalised O_acc / lr
+        const float fo = any ? f * (l_run / lr_run) : 0.f;
+        float* orow = p.o_part + row_idx * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(lane_addr + C::O_COL + cc * 32, o);
+            tmem_ld_wait(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (row_valid) {
+            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
+                                    __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+          }
+        }
+        if (row_valid) {
+          p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
+          p.l_out[lse_idx] = any ? l_run * f : 0.f;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool kBf16, int kMode>
+attn_status_t launch_prefill_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                     const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
+  using C = PrefillCfg<D>;
+  auto kern = prefill_kernel<D, kBf16, kMode>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+attn_status_t launch_prefill_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                      const CUtensorMap& mv, int mode, bool bf16, dim3 grid, cudaStream_t s) {
+  if (bf16) {
+    switch (mode) {
+      case kModeDense: return launch_prefill_variant<D, true, kModeDense>(p, mq, mk, mv, grid, s);
+      case kModePartial: return launch_prefill_variant<D, true, kModePartial>(p, mq, mk, mv, grid, s);
+      case kModeJagged: return launch_prefill_variant<D, true, kModeJagged>(p, mq, mk, mv, grid, s);
+    }
+  } else {
+    switch (mode) {
+      case kModeDense: return launch_prefill_variant<D, false, kModeDense>(p, mq, mk, mv, grid, s);
+      case kModePartial: return launch_prefill_variant<D, false, kModePartial>(p, mq, mk, mv, grid, s);
+      case kModeJagged: return launch_prefill_variant<D, false, kModeJagged>(p, mq, mk, mv, grid, s);
+    }
+  }
+  return ATTN_ERR_INVALID_ARG;
+}
+
+inline unsigned int prefill_take_status_impl(cudaStream_t s) {
+  if (cudaStreamSynchronize(s) != cudaSuccess) return kStatusTimeout;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_prefill_status, sizeof(v)) != cudaSuccess) return kStatusTimeout;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(zero));
+  }
+  return v;
+}
+
+}  // namespace attn

@@ -1,0 +1,138 @@
+// Flattened jagged worklist, built on the device from device-resident
+// seq_offsets (no host synchronisation).
+//
+// "[pallas] Support dependent Tile.end bounds in Pallas" ("Flattened
+// worklists"): a work item carries the resident source range
+// (range_start, range_len) and the compact Q tile (tile_start, tile_extent);
+// its compute end is min(source_end, compact_end).  The review thread on the
+// same page fixes the jagged KV end as seq_offsets[seq_idx + 1].
+//
+// Item = int4 {range_start, range_len, tile_start, tile_extent}, one per
+// (sequence, Q tile of block_m rows).  Order: sequences with more Q tiles
+// first (so long causal work starts early), sequences in index order within a
+// tile count, and inside a sequence its tiles from last to first (the last Q
+// tile has the longest causal KV walk).  When ceil(max_seqlen / block_m) > 64
+// the count buckets are skipped and sequences stay in index order.
+//
+// Output buffer: int count at word 0, items from byte 16.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+
+static __device__ unsigned int g_worklist_status;
+
+__global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restrict__ offs, int num_seqs,
+                                                        int total_tokens, int max_seqlen, int block_m,
+                                                        int* __restrict__ out, int max_items) {
+  int4* items = reinterpret_cast<int4*>(out + 4);
+  __shared__ int warp_sums[32];
+  __shared__ int s_base;
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int w = tid >> 5;
+  const int nmax = (max_seqlen + block_m - 1) / block_m;
+  const bool bucketed = nmax <= 64;
+  if (tid == 0) {
+    s_base = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  const int passes = bucketed ? nmax : 1;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int want = nmax - pass;  // tile count served by this pass (bucketed order)
+    for (int c0 = 0; c0 < num_seqs; c0 += 1024) {
+      const int b = c0 + tid;
+      int begin = 0, len = 0, nt = 0;
+      if (b < num_seqs) {
+        begin = offs[b];
+        const int end = offs[b + 1];
+        len = end - begin;
+        if (begin < 0 || end > total_tokens || len < 0 || len > max_seqlen) {
+          s_bad = 1;
+          len = 0;
+        }
+        nt = (len + block_m - 1) / block_m;
+      }
+      const bool take = bucketed ? (nt == want && nt > 0) : (nt > 0);
+      const int cnt = take ? nt : 0;
+      // block-wide exclusive scan of cnt
+      int x = cnt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+      }
+      if (lane == 31) warp_sums[w] = x;
+      __syncthreads();
+      if (w == 0) {
+        int y = warp_sums[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int z = __shfl_up_sync(0xffffffffu, y, d);
+          if (lane >= d) y += z;
+        }
+        warp_sums[lane] = y;
+      }
+      __syncthreads();
+      const int excl = x - cnt + (w > 0 ? warp_sums[w - 1] : 0);
+      const int total = warp_sums[31];
+      const int base = s_base;
+      if (take) {
+        for (int t = 0; t < nt; ++t) {
+          const long long pos = (long long)base + excl + (nt - 1 - t);
+          if (pos < max_items) {
+            const int tile_start = begin + t * block_m;
+            const int extent = min(block_m, len - t * block_m);
+            items[pos] = make_int4(begin, len, tile_start, extent);
+          }
+        }
+      }
+      __syncthreads();
+      if (tid == 0) s_base = base + total;
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    const int count = s_base < max_items ? s_base : max_items;
+    out[0] = count;
+    if (s_bad || s_base > max_items) atomicOr(&g_worklist_status, kStatusDeviceInput);
+  }
+}
+
+attn_status_t launch_worklist(const int32_t* seq_offsets, int num_seqs, int total_tokens, int max_seqlen, int block_m,
+                              int* count_and_items, int max_items, cudaStream_t s) {
+  worklist_kernel<<<1, 1024, 0, s>>>(seq_offsets, num_seqs, total_tokens, max_seqlen, block_m, count_and_items,
+                                     max_items);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// One thread waits, bounded, on a barrier that nothing completes.
+__global__ void selftest_timeout_kernel(uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  mbar_wait_bounded(&bar, 0, &abort_flag, &g_worklist_status, kStatusTimeout | (0xA0u << kStatusSiteShift),
+                    timeout_ns);
+}
+
+attn_status_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t s) {
+  selftest_timeout_kernel<<<1, 1, 0, s>>>(timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+unsigned int worklist_take_status(cudaStream_t s) {
+  if (cudaStreamSynchronize(s) != cudaSuccess) return kStatusTimeout;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_worklist_status, sizeof(v)) != cudaSuccess) return kStatusTimeout;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_worklist_status, &zero, sizeof(zero));
+  }
+  return v;
+}
+
+}  // namespace attn

@@ -1,0 +1,295 @@
+"""GPU parity: every entry point against the fp64 oracle, element by element.
+
+Tolerance (fixed for fp16/bf16 inputs, fp32 accumulation): max |O - O_ref| <= 1e-2,
+mean |O - O_ref| <= 1e-3, |LSE - LSE_ref| <= 1e-3; -inf LSE and empty rows must
+match exactly; integer outputs (worklists) bit-exact.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import ring_attention_online_gb300 as ra
+import synthetic as syn
+from oracle import attention as A
+from oracle import schedule as S
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN, TOL_LSE = 1e-2, 1e-3, 1e-3
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    ra.load_library()
+    yield
+    assert ra.attn_last_device_status() == 0
+
+
+def close_o(got, ref, what=""):
+    g = got.detach().float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (what, g.shape, ref.shape)
+    assert np.isfinite(g).all(), what
+    err = np.abs(g - ref)
+    assert err.max() <= TOL_MAX, f"{what}: max err {err.max():.3e}"
+    assert err.mean() <= TOL_MEAN, f"{what}: mean err {err.mean():.3e}"
+
+
+def close_lse(got, ref, what=""):
+    g = got.detach().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    neg = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(g), neg), what
+    if (~neg).any():
+        err = np.abs(g[~neg] - ref[~neg])
+        assert err.max() <= TOL_LSE, f"{what}: LSE err {err.max():.3e}"
+
+
+def gen(shape_q, shape_kv, dtype, seed):
+    return syn.qkv(shape_q, shape_kv, dtype, seed, "cuda")
+
+
+# ---------------------------------------------------------------------- prefill
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_dense_ragged(D, dtype, causal):
+    B, S_, h_q, h_kv = 2, 300, 4, 2
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), dtype, seed=D + causal)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    scale = 1 / math.sqrt(D)
+    ra.attn_prefill(q, k, v, o, lse, scale=scale, causal=causal)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), scale, causal)
+    close_o(o, O, f"prefill D={D} {dtype} causal={causal}")
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("C", [2, 3, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_ring_gqa(C, causal):
+    B, S_, h_q, h_kv, D = 1, 1000, 8, 2, 128
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=10 + C)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), causal)
+    close_o(o, O, f"ring C={C}")
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("S_q,S_kv", [(200, 700), (700, 200), (1, 513), (129, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_unequal_lengths(S_q, S_kv, causal):
+    q, k, v = gen((1, S_q, 2, 64), (1, S_kv, 1, 64), "bf16", seed=S_q)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, S_q, device="cuda", dtype=torch.float32)
+    ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=2)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / 8, causal)
+    close_o(o, O)
+    close_lse(lse, L)
+
+
+def test_prefill_empty_kv_gives_zero_and_neg_inf():
+    q, k, v = gen((1, 130, 2, 64), (1, 0, 2, 64), "bf16", seed=3)
+    k = torch.empty(1, 1, 2, 64, device="cuda", dtype=torch.bfloat16)  # any valid pointer
+    o = torch.full_like(q, 7.0)
+    lse = torch.zeros(1, 2, 130, device="cuda")
+    lib = ra.load_library()
+    import ctypes
+    st = lib.attn_prefill(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                          ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(lse.data_ptr()), 1, 130, 0, 2, 2, 64, 1,
+                          0.125, 1, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+# ---------------------------------------------------------------------- partial + merge
+def test_tiny_config_partials_merge_and_ring():
+    """B=1, h_q=2, h_kv=1, S=256, D=64, fp16, non-causal, C=4 chunks of 64 keys."""
+    cfg = syn.WORKLOADS["tiny_gqa_ring4"]
+    q, k, v = syn.prefill_inputs(cfg, seed=0, device="cuda")
+    B, S_, h_q, D, C = cfg["B"], cfg["S_q"], cfg["h_q"], cfg["D"], cfg["num_chunks"]
+    scale = 1 / math.sqrt(D)
+    m = torch.empty(C, B, h_q, S_, device="cuda")
+    l = torch.empty_like(m)
+    o_un = torch.empty(C, B, S_, h_q, D, device="cuda")
+    for c in range(C):
+        ra.attn_partial(q, k, v, m[c], l[c], o_un[c], scale=scale, causal=False, kv_begin=64 * c, kv_end=64 * (c + 1))
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    for c in range(C):
+        mr, lr, orr = A.partial(qc, kc, vc, scale, False, 0, 64 * c, 64 * (c + 1))
+        assert np.abs(m[c].cpu().numpy() - mr).max() <= 1e-3
+        assert np.abs(l[c].cpu().numpy() / lr - 1).max() <= 1e-3
+        close_o(o_un[c] / l[c].permute(0, 2, 1)[..., None], orr / np.swapaxes(lr, 1, 2)[..., None], f"partial {c}")
+    out = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda")
+    ra.attn_merge(m, l, o_un, out, lse)
+    O, L = A.attention(qc, kc, vc, scale, False)
+    close_o(out, O, "merge")
+    close_lse(lse, L)
+    o2 = torch.empty_like(q)
+    lse2 = torch.empty_like(lse)
+    ra.attn_prefill(q, k, v, o2, lse2, scale=scale, causal=False, num_chunks=C)
+    close_o(o2, O, "ring prefill")
+    close_lse(lse2, L)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_partial_causal_positions_and_identity(D):
+    B, S_q, S_kv, h = 1, 160, 600, 2
+    q, k, v = gen((B, S_q, h, D), (B, S_kv, h, D), "bf16", seed=D)
+    scale = 1 / math.sqrt(D)
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    # queries at positions 300..459 against keys [250, 520): partly visible, row by row
+    m = torch.empty(B, h, S_q, device="cuda")
+    l = torch.empty_like(m)
+    o = torch.empty(B, S_q, h, D, device="cuda")
+    ra.attn_partial(q, k, v, m, l, o, scale=scale, causal=True, q_pos0=300, kv_begin=250, kv_end=520)
+    mr, lr, orr = A.partial(qc, kc, vc, scale, True, 300, 250, 520)
+    assert np.abs(m.cpu().numpy() - mr).max() <= 1e-3
+    assert np.abs(l.cpu().numpy() / lr - 1).max() <= 1e-3
+    close_o(o / l.permute(0, 2, 1)[..., None], orr / np.swapaxes(lr, 1, 2)[..., None])
+    # queries at positions 0..159 against keys [400, 600): nothing visible -> identity
+    ra.attn_partial(q, k, v, m, l, o, scale=scale, causal=True, q_pos0=0, kv_begin=400, kv_end=600)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isneginf(m)) and torch.all(l == 0) and torch.all(o == 0)
+    # empty range -> identity
+    ra.attn_partial(q, k, v, m, l, o, scale=scale, causal=False, kv_begin=17, kv_end=17)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isneginf(m)) and torch.all(l == 0) and torch.all(o == 0)
+
+
+def test_merge_with_empty_partials_matches_full():
+    B, S_, h, D = 2, 70, 3, 128
+    q, k, v = gen((B, S_, h, D), (B, S_, h, D), "bf16", seed=5)
+    scale = 1 / math.sqrt(D)
+    bounds = [(0, 10), (10, 10), (10, 69), (69, 70), (70, 70)]
+    C = len(bounds)
+    m = torch.empty(C, B, h, S_, device="cuda")
+    l = torch.empty_like(m)
+    o_un = torch.empty(C, B, S_, h, D, device="cuda")
+    for c, (lo, hi) in enumerate(bounds):
+        ra.attn_partial(q, k, v, m[c], l[c], o_un[c], scale=scale, causal=True, kv_begin=lo, kv_end=hi)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, h, S_, device="cuda")
+    ra.attn_merge(m, l, o_un, out, lse)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), scale, True)
+    close_o(out, O)
+    close_lse(lse, L)
+
+
+# ---------------------------------------------------------------------- jagged
+def _jagged_case(lengths, H, D, seed, causal=True):
+    offs = syn.offsets_from_lengths(lengths)
+    T = int(offs[-1])
+    q, k, v = syn.qkv((T, H, D), (T, H, D), "bf16", seed, "cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(H, T, device="cuda")
+    max_len = int(max(lengths)) if len(lengths) else 0
+    ws = torch.empty(ra.attn_jagged_workspace_bytes(len(lengths), T, max_len), dtype=torch.uint8, device="cuda")
+    offs_d = torch.from_numpy(offs).cuda()
+    ra.attn_jagged(q, k, v, o, offs_d, max_len, ws, lse, causal=causal)
+    return q, k, v, o, lse, offs, ws
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_jagged_parity_and_worklist(causal):
+    lengths = [0, 1, 5, 127, 128, 129, 300, 1024, 77, 0, 256, 640]
+    H, D = 2, 128
+    q, k, v, o, lse, offs, ws = _jagged_case(lengths, H, D, seed=21, causal=causal)
+    O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), causal)
+    close_o(o, O)
+    close_lse(lse, L)
+    # worklist: the same items as the oracle's flattened worklist, bit for bit
+    words = ws.view(torch.int32).cpu().numpy()
+    count = int(words[0])
+    items = words[4:4 + 4 * count].reshape(count, 4)
+    ref = S.jagged_worklist(offs, 128, 128, causal)
+    assert count == len(ref)
+    got = sorted(map(tuple, items.tolist()))
+    want = sorted((it["ordered_begin"], it["range_len"], it["tile_start"], it["tile_extent"]) for it in ref)
+    assert got == want
+    # order: non-increasing Q-tile count per sequence, and each sequence's tiles last-to-first
+    ntiles = [(r[1] + 127) // 128 for r in items]
+    assert all(a >= b for a, b in zip(ntiles, ntiles[1:]))
+    for a, b in zip(items, items[1:]):
+        if a[0] == b[0]:
+            assert b[2] == a[2] - 128
+
+
+def test_jagged_random_lengths():
+    rng = np.random.default_rng(3)
+    lengths = rng.integers(0, 700, 40)
+    q, k, v, o, lse, offs, _ = _jagged_case(lengths, 4, 64, seed=22)
+    O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / 8, True)
+    close_o(o, O)
+    close_lse(lse, L)
+
+
+# ---------------------------------------------------------------------- decode
+@pytest.mark.parametrize("D,h_q,h_kv,S_kv,splits", [
+    (128, 16, 2, 5000, 7),     # G = 8, uneven splits, ragged tail
+    (128, 16, 1, 4096, 64),    # G = 16
+    (128, 4, 4, 777, 3),       # MHA, G = 1
+    (64, 8, 1, 3000, 5),
+    (256, 8, 2, 2000, 4),
+    (128, 8, 1, 100, 16),      # more splits than 64-key tiles: empty chunks
+])
+def test_decode_parity_and_partials(D, h_q, h_kv, S_kv, splits):
+    B = 2
+    q, k, v = syn.qkv((B, h_q, D), (B, S_kv, h_kv, D), "bf16", S_kv + D, "cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, device="cuda")
+    ws = torch.empty(ra.attn_decode_workspace_bytes(B, h_q, D, splits), dtype=torch.uint8, device="cuda")
+    scale = 1 / math.sqrt(D)
+    ra.attn_decode_splitkv(q, k, v, o, ws, lse, num_splits=splits, scale=scale)
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    O, L = A.decode(qc, kc, vc, scale, splits)
+    close_o(o, O)
+    close_lse(lse, L)
+    # the partial triplets in the documented workspace layout
+    rows = splits * B * h_q
+    f = ws.view(torch.float32)
+    m = f[:rows].view(splits, B, h_q).cpu().numpy()
+    l = f[rows:2 * rows].view(splits, B, h_q).cpu().numpy()
+    off = ((rows * 8 + 15) // 16) * 4
+    ou = f[off:off + rows * D].view(splits, B, h_q, D).cpu().numpy()
+    mr, lr, orr = A.decode_partials(qc, kc, vc, scale, splits)
+    empty = np.isneginf(mr)
+    assert np.array_equal(np.isneginf(m), empty)
+    assert np.all(l[empty] == 0) and np.all(ou[empty] == 0)
+    assert np.abs(m[~empty] - mr[~empty]).max() <= 1e-3
+    assert np.abs(l[~empty] / lr[~empty] - 1).max() <= 1e-3
+    norm = ou[~empty] / l[~empty][:, None]
+    ref_norm = orr[~empty] / lr[~empty][:, None]
+    assert np.abs(norm - ref_norm).max() <= TOL_MAX
+
+
+# ---------------------------------------------------------------------- failure detection
+def test_bounded_wait_times_out_cleanly_and_context_survives():
+    assert ra.attn_last_device_status() == 0
+    ra.attn_selftest_wait_timeout(20_000_000)  # 20 ms
+    assert ra.attn_last_device_status() == 4   # ATTN_ERR_TIMEOUT, reported once
+    assert ra.attn_last_device_status() == 0
+    q, k, v = gen((1, 64, 1, 64), (1, 64, 1, 64), "bf16", seed=1)
+    o = torch.empty_like(q)
+    ra.attn_prefill(q, k, v, o, causal=True)
+    O, _ = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / 8, True)
+    close_o(o, O)
+
+
+def test_malformed_offsets_reported_as_device_input_error():
+    offs = torch.tensor([0, 50, 30, 80], dtype=torch.int32, device="cuda")  # sequence 1 has negative length
+    q = torch.randn(80, 1, 64, device="cuda").bfloat16()
+    o = torch.zeros_like(q)
+    ws = torch.empty(ra.attn_jagged_workspace_bytes(3, 80, 64), dtype=torch.uint8, device="cuda")
+    ra.attn_jagged(q, q, q, o, offs, 64, ws)
+    assert ra.attn_last_device_status() == 5
+    assert ra.attn_last_device_status() == 0
