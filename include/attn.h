@@ -163,6 +163,29 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, v
 size_t attn_decode_workspace_bytes(int B, int h_q, int D, int num_splits);
 
 /*
+ * attn_decode_splitkv_noalloc - attn_decode_splitkv without a workspace argument,
+ * for callers that cannot allocate device memory: a program whose device memory is
+ * owned by a host framework that gives it only its inputs and outputs, or a
+ * latency-critical loop that must not call cudaMalloc/cudaFree (they can
+ * synchronise the device) nor risk running out of memory mid-run.  No counterpart
+ * on the pages: it only changes where the scratch lives.
+ *
+ * The partial triplets go to a fixed array of ATTN_NOALLOC_SCRATCH_BYTES in device
+ * memory that is part of the library (present on every GPU that loads it, until
+ * the process exits).  Nothing is allocated or freed.  Same arguments, layouts and
+ * results as attn_decode_splitkv.  Returns ATTN_ERR_UNSUPPORTED when the partials,
+ * attn_decode_workspace_bytes(B, h_q, D, num_splits), exceed the array.
+ * The first call on a device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.  All calls share the
+ * array and it keeps the last call's contents (every entry a call reads is written
+ * by that call first); calls whose kernels overlap on the GPU race on it.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                          int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale,
+                                          int num_splits, attn_stream_t stream);
+
+/*
  * attn_last_device_status - synchronise `stream`, then return and clear the
  * device-side status (ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_INPUT) raised by any
  * kernel of the library since the previous call; ATTN_OK if none.

@@ -21,7 +21,7 @@ import os
 __all__ = [
     "AttnError", "load_library", "library_path",
     "attn_prefill", "attn_partial", "attn_merge", "attn_jagged", "attn_decode_splitkv",
-    "attn_jagged_workspace_bytes", "attn_decode_workspace_bytes",
+    "attn_jagged_workspace_bytes", "attn_decode_workspace_bytes", "attn_decode_splitkv_noalloc",
     "attn_last_device_status", "attn_status_string", "attn_tile_walk", "attn_selftest_wait_timeout",
     "BLOCK_M", "BLOCK_N", "STATUS",
 ]
@@ -55,6 +55,7 @@ _SIGNATURES = {
     "attn_jagged_workspace_bytes": [_I, _I, _I],
     "attn_decode_splitkv": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P],
     "attn_decode_workspace_bytes": [_I, _I, _I, _I],
+    "attn_decode_splitkv_noalloc": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P],
     "attn_last_device_status": [_P],
     "attn_status_string": [_I],
     "attn_tile_walk": [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P],
@@ -185,6 +186,18 @@ def attn_decode_splitkv(q, k, v, o, workspace, lse=None, *, num_splits, scale=No
                                             _dtype_code(q), _scale(scale, D), int(num_splits), _ptr(workspace),
                                             workspace.numel() * workspace.element_size(), _stream(stream, q))
     _check(st, "attn_decode_splitkv")
+
+
+def attn_decode_splitkv_noalloc(q, k, v, o, lse=None, *, num_splits, scale=None, stream=None):
+    """attn_decode_splitkv with the partials in the library's fixed device scratch, for
+    callers that cannot allocate device memory (see attn.h for its limit and sharing rules)."""
+    _cuda_contig(q, k, v, o, lse)
+    B, h_q, D = q.shape
+    S_kv, h_kv = k.shape[1], k.shape[2]
+    st = load_library().attn_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_kv, h_q,
+                                                    h_kv, D, _dtype_code(q), _scale(scale, D), int(num_splits),
+                                                    _stream(stream, q))
+    _check(st, "attn_decode_splitkv_noalloc")
 
 
 def attn_last_device_status(stream=None) -> int:

@@ -1,0 +1,60 @@
+// Split-KV decode for callers that cannot allocate device memory.
+//
+// attn_decode_splitkv needs a caller-provided workspace for the per-chunk
+// partial triplets.  Some callers have no way to provide one: a host program
+// whose memory is owned by a framework that hands plugins only their input and
+// output buffers, or a latency-critical loop that must never call cudaMalloc /
+// cudaFree (both can synchronise the whole device) and must not risk an
+// out-of-memory failure in the middle of a run.  For them this file keeps the
+// scratch in a fixed-size array in device memory that is part of the library
+// image: it exists on every GPU that loads the library, from load until the
+// process exits, and no call here allocates or frees anything.
+//
+// The array is shared by every call on a device and keeps whatever the last
+// call wrote.  Nothing needs to start at zero: the partial kernel writes every
+// (chunk, batch, head) triplet before the merge kernel reads it.  Two calls
+// whose kernels overlap on the GPU (e.g. on two streams) race on the array.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace attn {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mutex;
+
+// Device address of the scratch array on the current device.  The host-side
+// symbol g_decode_scratch is only a stand-in, not a device address, so it is
+// looked up once per device with that device current and cached.
+attn_status_t scratch_on_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                                     int B, int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype,
+                                                     float scale, int num_splits, attn_stream_t stream) {
+  if (B < 0 || h_q < 1 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_decode_workspace_bytes(B, h_q, D, num_splits);
+  if (need > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;  // partials do not fit the fixed scratch
+  void* scratch = nullptr;
+  const attn_status_t st = attn::scratch_on_current_device(&scratch);
+  if (st != ATTN_OK) return st;
+  return attn_decode_splitkv(q, k, v, o, lse, B, S_kv, h_q, h_kv, D, dtype, scale, num_splits, scratch,
+                             ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
