@@ -49,6 +49,18 @@ bool dtype_ok(attn_dtype_t d) { return d == ATTN_FP16 || d == ATTN_BF16; }
 bool scale_ok(float s) { return isfinite(s) && s > 0.f; }
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Head dims 64 and 128 run two 128-row Q sub-tiles per CTA (query heads h, h+1 of
+// one KV group when the group size is even, else Q tiles 2t, 2t+1 of one head);
+// head dim 256 runs one Q tile per CTA (two of its O tiles do not fit in TMEM).
+bool paired(int D) { return D <= 128; }
+int jagged_block(int D) { return paired(D) ? 2 * ATTN_BLOCK_M : ATTN_BLOCK_M; }
+
+dim3 dense_grid(const PrefillParams& p, int D) {
+  if (!paired(D)) return dim3((p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, p.h_q, p.B);
+  if (p.pair_heads) return dim3((p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, p.h_q / 2, p.B);
+  return dim3((p.S_q + 2 * ATTN_BLOCK_M - 1) / (2 * ATTN_BLOCK_M), p.h_q, p.B);
+}
+
 attn_status_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, int mode, bool bf16, int D, dim3 grid, cudaStream_t s) {
   switch (D) {
@@ -73,9 +85,9 @@ attn_status_t check_dense(const void* q, const void* k, const void* v, int B, in
   return ATTN_OK;
 }
 
-size_t jagged_max_items(int num_seqs, int total_tokens) {
-  // sum_b ceil(L_b / BM) <= (T + num_seqs * (BM - 1)) / BM
-  return ((size_t)total_tokens + (size_t)num_seqs * (ATTN_BLOCK_M - 1)) / ATTN_BLOCK_M;
+size_t jagged_max_items(int num_seqs, int total_tokens, int block_m = ATTN_BLOCK_M) {
+  // sum_b ceil(L_b / block_m) <= (T + num_seqs * (block_m - 1)) / block_m
+  return ((size_t)total_tokens + (size_t)num_seqs * (block_m - 1)) / block_m;
 }
 
 }  // namespace
@@ -109,12 +121,12 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   p.kv_lo = 0;
   p.kv_hi = S_kv;
   p.scale_log2 = scale * kLog2e;
+  p.pair_heads = (p.group % 2) == 0;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  const dim3 grid((S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, h_q, B);
-  return launch_prefill(p, mq, mk, mv, kModeDense, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
+  return launch_prefill(p, mq, mk, mv, kModeDense, bf16, D, dense_grid(p, D), reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o_unnorm,
@@ -143,12 +155,12 @@ attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m
   p.kv_lo = kv_begin;
   p.kv_hi = kv_end;
   p.scale_log2 = scale * kLog2e;
+  p.pair_heads = (p.group % 2) == 0;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  const dim3 grid((S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, h_q, B);
-  return launch_prefill(p, mq, mk, mv, kModePartial, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
+  return launch_prefill(p, mq, mk, mv, kModePartial, bf16, D, dense_grid(p, D), reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, int C, int B, int S_q, int H, int D,
@@ -182,11 +194,12 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
   if (num_seqs == 0 || total_tokens == 0) return ATTN_OK;
   if (!workspace || !aligned(workspace, 16) || workspace_bytes < attn_jagged_workspace_bytes(num_seqs, total_tokens, max_seqlen))
     return ATTN_ERR_INVALID_ARG;
-  const size_t max_items = jagged_max_items(num_seqs, total_tokens);
+  const int block = jagged_block(D);
+  const size_t max_items = jagged_max_items(num_seqs, total_tokens, block);
   if (max_items > 0x7fffffffULL || H > 65535) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* wl = static_cast<int*>(workspace);
-  st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, ATTN_BLOCK_M, wl, (int)max_items, s);
+  st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, block, wl, (int)max_items, s);
   if (st != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
   PrefillParams p{};

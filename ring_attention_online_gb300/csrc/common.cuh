@@ -33,6 +33,7 @@ struct PrefillParams {
   // sizes (jagged: B = 1, S_q = S_kv = total_tokens, h_q = h_kv = H)
   int B, S_q, S_kv, h_q, h_kv, group;
   int causal, num_chunks;
+  int pair_heads;  // paired kernel: the two Q sub-tiles are heads (h, h+1) at one Q tile (else Q tiles 2t, 2t+1)
   int q_pos0, kv_pos0, kv_lo, kv_hi;  // dense / partial key range and positions
   float scale_log2;                   // softmax scale * log2(e)
   // jagged worklist: count followed by items {seq_begin, seq_len, tile_start, tile_extent}

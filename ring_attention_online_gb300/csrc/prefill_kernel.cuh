@@ -12,14 +12,15 @@
 //    at min(kv_end, tile_q.end) (no fully masked tile is visited); only the
 //    diagonal and tail tiles are masked.
 //
-// CTA layout (192 threads):
+// CTA layout (320 threads):
 //   warp 0      TMA producer: Q tile once, then K/V 128-column slabs through a
 //               ring of NST shared-memory stages, in the order the MMA needs.
 //   warp 1      TMEM owner and single-thread tcgen05 issuer:
 //               S(0), then per tile j: S(j+1), PV(j).  S(j) = Q.K_j^T goes to one
 //               of two 128-column TMEM buffers; PV(j) reads P(j) (bf16/fp16,
 //               written over S(j) by the softmax warps) as the TMEM A operand.
-//   warps 2..5  softmax + epilogue, one query row per thread (TMEM lane).
+//   warps 2..9  softmax + epilogue: each query row (TMEM lane) is shared by two
+//               warps, one per half of the tile's 128 keys and of O's columns.
 //               Scores are scaled into the exp2 domain; the running max is
 //               raised lazily (only when it grows by more than 2^8), so O is
 //               rescaled in TMEM only on those tiles - the result is the same
@@ -32,13 +33,9 @@
 
 #include <math_constants.h>
 
-#include "common.cuh"
-#include "ptx.cuh"
-#include "schedule.cuh"
+#include "prefill_common.cuh"
 
 namespace attn {
-
-static __device__ unsigned int g_prefill_status;
 
 template <int D>
 struct PrefillCfg {
@@ -50,45 +47,22 @@ struct PrefillCfg {
   static constexpr int BLOCK_BYTES = 128 * 128; // one TMA block: 128 rows x 128 bytes
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int SLAB_BYTES = BN * SC * 2;
-  static constexpr int DATA_BUDGET = 224 * 1024;
-  static constexpr int NST = (DATA_BUDGET - Q_BYTES) / SLAB_BYTES;
+  // four K/V slabs in flight: on GB300 two to six stages time the same, so
+  // the rest of shared memory stays free for the softmax warps' exchanges
+  static constexpr int NST = D == 64 ? 8 : 4;
   static constexpr int SMEM_BYTES = Q_BYTES + NST * SLAB_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   // S(j) / P(j) live in TMEM columns [128*(j%2), 128*(j%2)+128); O after them
   static constexpr uint32_t O_COL = 256;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;  // TMA warp, MMA warp, 8 softmax warps
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(NST >= 2, "at least two K/V stages");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-// Bounded wait used by every role; also gives up as soon as another CTA of
-// any launch has reported a timeout (so a broken pipeline ends quickly).
-__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort, uint32_t site) {
-  if (mbar_try_wait(smem_u32(bar), parity)) return true;
-  if (*reinterpret_cast<volatile unsigned int*>(&g_prefill_status) & kStatusTimeout) {
-    *abort = 1u;
-    return false;
-  }
-  return mbar_wait_bounded(bar, parity, abort, &g_prefill_status, kStatusTimeout | (site << kStatusSiteShift),
-                           kWaitTimeoutNs);
-}
-
-// Wait used only while tearing down after an abort: ignores the abort flag.
-__device__ __forceinline__ void pf_drain(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(a, parity)) {
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-      atomicOr(&g_prefill_status, kStatusTimeout | (0x80u << kStatusSiteShift));
-      return;
-    }
-  }
-}
-
 template <int D, bool kBf16, int kMode>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = PrefillCfg<D>;
@@ -98,6 +72,10 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ uint64_t bar_s[2], bar_p[2];
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
+  __shared__ float xch_max[2][2][128];  // [tile parity][column half][row]
+  __shared__ float xch_l[2][128], xch_lr[2][128];
+  __shared__ uint64_t bar_x[2][4];       // pair exchange barriers: [tile parity][lane quarter]
+  __shared__ uint64_t bar_xe[4];         // end-of-row exchange barrier per lane quarter
 
   // ------------------------------------------------------------ work item
   int b, h, q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0;
@@ -147,8 +125,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
-      mbar_init(&bar_p[i], 128);
+      mbar_init(&bar_p[i], 256);
+      for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 64);
     }
+    for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_xe[q4], 64);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -278,20 +258,27 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ========================================================== softmax + epilogue
+    // Two warps share each TMEM lane quarter: warp (2 + wq) and (6 + wq) ... take
+    // the two column halves of every row (keys [64*half, 64*half + 64) of a tile,
+    // O columns [half*D/2, half*D/2 + D/2)).  The pair exchanges row maxima once per
+    // tile through shared memory, so both halves take identical decisions.
+    const int sw = warp - 2;  // 0..7
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = sw >> 2;
     const int row = wq * 32 + lane;
     const int q_row = q_lo + row;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    constexpr int HD = D / 2;                                    // O columns per half
     const float c = p.scale_log2;  // > 0
     float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
-    float l_run = 0.f;             // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
-    float lr_run = 0.f;            // sum of the rounded P the MMA multiplies V by: normalises O
+    float l_run = 0.f;             // this half's sum of exp2(x - m_run) in fp32: l and LSE
+    float lr_run = 0.f;            // this half's sum of the rounded P the MMA multiplies V by
     float m_max = -CUDART_INF_F;   // true running max (partial mode)
     bool ok = true;
-    TileWalk sw = walk;
+    TileWalk sw_walk = walk;
     for (int j = 0; j < n; ++j) {
       int ch, kstart, mend;
-      sw.next(ch, kstart, mend);
+      sw_walk.next(ch, kstart, mend);
       const int buf = j & 1;
       if (!pf_wait(&bar_s[buf], (uint32_t)((j >> 1) & 1), &abort_flag, 6)) {
         ok = false;
@@ -299,41 +286,48 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after_sync();
       const uint32_t scol = lane_addr + static_cast<uint32_t>(buf * 128);
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(scol, r0);
-      tmem_ld32(scol + 32, r1);
-      tmem_ld32(scol + 64, r2);
-      tmem_ld32(scol + 96, r3);
+      uint32_t r0[32], r1[32];
+      tmem_ld32(scol + half * 64, r0);
+      tmem_ld32(scol + half * 64 + 32, r1);
       tmem_ld_wait(r0);
       tmem_ld_wait(r1);
-      tmem_ld_wait(r2);
-      tmem_ld_wait(r3);
 
-      // mask the diagonal / tail tile: key kstart+i is visible iff i < lim
+      // mask the diagonal / tail tile: key kstart + i is visible iff i < lim
       const bool need_mask =
           (kstart + C::BN > mend) ||
           (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo));
       if (need_mask) {
-        int lim = mend - kstart;
+        long long lim = (long long)mend - kstart;
         if (p.causal) {
           const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
-          lim = (int)(lc < lim ? lc : lim);
+          lim = lc < lim ? lc : lim;
         }
+        const long long lh = lim - half * 64;  // limit within this half
         const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (i >= lim) r0[i] = ninf;
-          if (i + 32 >= lim) r1[i] = ninf;
-          if (i + 64 >= lim) r2[i] = ninf;
-          if (i + 96 >= lim) r3[i] = ninf;
+          if (i >= lh) r0[i] = ninf;
+          if (i + 32 >= lh) r1[i] = ninf;
         }
       }
-      float mx = -CUDART_INF_F;
+      float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r1[i])),
-                             fmaxf(__uint_as_float(r2[i]), __uint_as_float(r3[i]))));
+      for (int i = 0; i < 8; ++i)
+        mx8[i] = fmaxf(fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8])),
+                             fmaxf(__uint_as_float(r0[i + 16]), __uint_as_float(r0[i + 24]))),
+                       fmaxf(fmaxf(__uint_as_float(r1[i]), __uint_as_float(r1[i + 8])),
+                             fmaxf(__uint_as_float(r1[i + 16]), __uint_as_float(r1[i + 24]))));
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // both halves of the row see each other's max (the S(j) columns are all in
+      // registers by now, so P may overwrite them after this barrier)
+      xch_max[buf][half][row] = mx;
+      mbar_arrive(&bar_x[buf][wq]);
+      if (!pf_wait(&bar_x[buf][wq], (uint32_t)((j >> 1) & 1), &abort_flag, 9)) {
+        ok = false;
+        break;
       }
+      mx = fmaxf(mx, xch_max[buf][half ^ 1][row]);
       const float m_tile = mx * c;  // -inf when the whole row is masked
       if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
       const float m_new = fmaxf(m_run, m_tile);
@@ -346,7 +340,7 @@ __global__ void __launch_bounds__(192, 1)
         lr_run *= alpha;
       }
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
-      float sum = 0.f, sum_r = 0.f;
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sr[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[16];
       auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
 #pragma unroll
@@ -354,21 +348,19 @@ __global__ void __launch_bounds__(192, 1)
           const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), c, neg_m));
           const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), c, neg_m));
           pk[i] = pack_half2<kBf16>(p0, p1);
-          sum += p0 + p1;
+          sa[i & 3] += p0 + p1;
           // O is normalised by the sum of the rounded weights it was built
           // from, so O / l is a weighted mean with consistent weights
           const float2 pr = unpack_half2<kBf16>(pk[i]);
-          sum_r += pr.x + pr.y;
+          sr[i & 3] += pr.x + pr.y;
         }
         tmem_st16(scol + col, pk);
       };
-      // P(j) overwrites the first 64 columns of S(j), already in registers
-      pack_chunk(r0, 0);
-      pack_chunk(r1, 16);
-      pack_chunk(r2, 32);
-      pack_chunk(r3, 48);
-      l_run += sum;
-      lr_run += sum_r;
+      // P(j) for keys [64*half, 64*half+64) goes to columns [32*half, 32*half+32)
+      pack_chunk(r0, half * 32);
+      pack_chunk(r1, half * 32 + 16);
+      l_run += (sa[0] + sa[1]) + (sa[2] + sa[3]);
+      lr_run += (sr[0] + sr[1]) + (sr[2] + sr[3]);
 
       if (j > 0) {
         // PV(j-1) must be complete before O is rescaled (and it keeps the
@@ -380,13 +372,14 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after_sync();
         if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < HD / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld32(lane_addr + C::O_COL + cc * 32, o);
+            const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
+            tmem_ld32(oa, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_addr + C::O_COL + cc * 32, o);
+            tmem_st32(oa, o);
           }
         }
       }
@@ -398,6 +391,13 @@ __global__ void __launch_bounds__(192, 1)
       ok = pf_wait(&bar_o, (uint32_t)((n - 1) & 1), &abort_flag, 8);
       tc_fence_after_sync();
     }
+    // the row's sums are split over the two halves
+    xch_l[half][row] = l_run;
+    xch_lr[half][row] = lr_run;
+    mbar_arrive(&bar_xe[wq]);
+    if (ok) ok = pf_wait(&bar_xe[wq], 0, &abort_flag, 10);
+    l_run += xch_l[half ^ 1][row];
+    lr_run += xch_lr[half ^ 1][row];
     if (ok) {
       const bool row_valid = q_row < q_hi;
       const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
@@ -405,12 +405,12 @@ __global__ void __launch_bounds__(192, 1)
       constexpr float kLn2 = 0.693147180559945309f;
       if constexpr (kMode != kModePartial) {
         const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
-        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + half * HD;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           uint32_t o[32];
           if (n > 0) {
-            tmem_ld32(lane_addr + C::O_COL + cc * 32, o);
+            tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
             tmem_ld_wait(o);
           } else {
 #pragma unroll
@@ -426,19 +426,19 @@ __global__ void __launch_bounds__(192, 1)
             for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
           }
         }
-        if (p.lse != nullptr && row_valid)
+        if (p.lse != nullptr && row_valid && half == 0)
           p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
       } else {
         const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
         const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
         // O re-weighted so that O / l equals the consistently normalised O_acc / lr
         const float fo = any ? f * (l_run / lr_run) : 0.f;
-        float* orow = p.o_part + row_idx * D;
+        float* orow = p.o_part + row_idx * D + half * HD;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           uint32_t o[32];
           if (n > 0) {
-            tmem_ld32(lane_addr + C::O_COL + cc * 32, o);
+            tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
             tmem_ld_wait(o);
           } else {
 #pragma unroll
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(192, 1)
                                     __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
           }
         }
-        if (row_valid) {
+        if (row_valid && half == 0) {
           p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
           p.l_out[lse_idx] = any ? l_run * f : 0.f;
         }
@@ -497,17 +497,6 @@ attn_status_t launch_prefill_dispatch(const PrefillParams& p, const CUtensorMap&
     }
   }
   return ATTN_ERR_INVALID_ARG;
-}
-
-inline unsigned int prefill_take_status_impl(cudaStream_t s) {
-  if (cudaStreamSynchronize(s) != cudaSuccess) return kStatusTimeout;
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_prefill_status, sizeof(v)) != cudaSuccess) return kStatusTimeout;
-  if (v != 0) {
-    const unsigned int zero = 0;
-    cudaMemcpyToSymbol(g_prefill_status, &zero, sizeof(zero));
-  }
-  return v;
 }
 
 }  // namespace attn

@@ -1,0 +1,543 @@
+// Blockwise online-softmax attention forward for head dimensions 64 and 128:
+// two 128-row Q sub-tiles per CTA that share every K/V tile.
+//
+// What it computes is the same as the single-tile kernel (prefill_kernel.cuh):
+// per KV tile, S = Q.K^T, the running (m, l, O) updated by online softmax
+// ("kernbench2 _gqa_prefill_long.py", step 0 partial and the ring-step merge),
+// O / l at the end, over the tiles of a ring-order walk that stops at
+// min(kv_end, tile_q.end) ("[pallas] Support dependent Tile.end bounds in
+// Pallas").  The difference is the amount of K/V traffic per FLOP: each K/V
+// byte brought into shared memory feeds 256 query rows instead of 128, which
+// halves what the TMA has to deliver per tensor-core cycle (one 128-row tile
+// needs ~64 B/clk/SM at full MMA rate, about the measured TMA ceiling).
+//
+// Pairing: for GQA the sub-tiles are two query heads of one KV group at the
+// same Q tile (identical tile walks); otherwise they are two consecutive Q
+// tiles of one head / sequence and share the walk of the later one, the
+// earlier sub-tile sitting out the tiles it cannot see (no masked-only work).
+//
+// CTA layout (320 threads):
+//   warp 0      TMA producer: both Q sub-tiles, then K(0), V(0), K(1), V(1), ...
+//               through a ring of NST stages (one stage = one K or V tile).
+//   warp 1      TMEM owner (512 columns: S_A, S_B, O_A, O_B) and single-thread
+//               tcgen05 issuer, in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
+//               PV_B(j) S_B(j+1) | ... so one sub-tile's MMAs run while the
+//               other sub-tile's softmax is computed.
+//   warps 2..5  softmax + epilogue of sub-tile A, one query row per thread.
+//   warps 6..9  the same for sub-tile B.
+// P(j) of a sub-tile (bf16/fp16) overwrites the first 64 columns of its S
+// buffer and is the TMEM A operand of P.V.  Every wait is bounded.
+#pragma once
+
+#include "prefill_common.cuh"
+
+namespace attn {
+
+template <int D>
+struct PairCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int BLOCK_BYTES = 128 * 128;  // one TMA block: 128 rows x 128 bytes
+  static constexpr int Q_BYTES = BM * D * 2;     // one sub-tile
+  static constexpr int SLAB_BYTES = BN * D * 2;  // one K or V tile
+  static constexpr int NST = (224 * 1024 - 2 * Q_BYTES) / SLAB_BYTES;
+  static constexpr int SMEM_BYTES = 2 * Q_BYTES + NST * SLAB_BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL = 256;  // S_A 0..127, S_B 128..255, O_A 256.., O_B 256+D..
+  static constexpr int THREADS = 320;
+  static_assert(D == 64 || D == 128, "paired kernel: head dim 64 or 128");
+  static_assert(NST >= 3, "K(j+1) must be loadable while K(j) and V(j) are held");
+  static_assert(SMEM_BYTES <= 227 * 1024 - 512, "shared memory budget");
+};
+
+struct SubTile {
+  int h, q_lo, q_hi;
+  __device__ bool empty() const { return q_hi <= q_lo; }
+};
+
+template <int D, bool kBf16, int kMode>
+// 10 warps put three on two of the four SM sub-partitions (16K registers
+// each), so at most 168 registers per thread
+__global__ void __launch_bounds__(320, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                        const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
+  using C = PairCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_fin;
+  __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
+  __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t abort_flag;
+
+  // ------------------------------------------------------------ work item
+  int b, kv_lo, kv_hi, q_pos0, kv_pos0;
+  SubTile st0, st1;
+  if constexpr (kMode == kModeJagged) {
+    const int item = blockIdx.x;
+    if (item >= *p.work_count) return;  // the grid is an upper bound on the item count
+    const int4 it = p.work_items[item];  // a 256-row Q tile of one sequence
+    b = 0;
+    const int h = blockIdx.y;
+    const int a_hi = it.z + min(it.w, C::BM);
+    st0 = SubTile{h, it.z, a_hi};
+    st1 = SubTile{h, a_hi, it.z + it.w};
+    kv_lo = it.x;
+    kv_hi = it.x + it.y;  // seq_offsets[seq_idx + 1]
+    q_pos0 = 0;
+    kv_pos0 = 0;
+  } else {
+    b = blockIdx.z;
+    kv_lo = p.kv_lo;
+    kv_hi = p.kv_hi;
+    q_pos0 = p.q_pos0;
+    kv_pos0 = p.kv_pos0;
+    // causal: longest Q tiles first, so the short ones fill the tail
+    const int t = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    if (p.pair_heads) {
+      const int lo = t * C::BM, hi = min(lo + C::BM, p.S_q);
+      st0 = SubTile{2 * (int)blockIdx.y, lo, hi};
+      st1 = SubTile{2 * (int)blockIdx.y + 1, lo, hi};
+    } else {
+      const int lo = t * 2 * C::BM;
+      const int mid = min(lo + C::BM, p.S_q), hi = min(lo + 2 * C::BM, p.S_q);
+      st0 = SubTile{(int)blockIdx.y, lo, mid};
+      st1 = SubTile{(int)blockIdx.y, mid, hi};
+    }
+  }
+  const int hk = st0.h / p.group;
+  const int u_lo = st0.q_lo;
+  const int u_hi = st1.empty() ? st0.q_hi : max(st0.q_hi, st1.q_hi);
+  TileWalk walk;
+  walk.init(u_lo, u_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, p.num_chunks, C::BN);
+  const int n = walk.count();
+  // sub-tile x takes part in the tile starting at key `ks` iff it has rows and
+  // (causal) its last query sees the tile's first key
+  auto sub = [&](int x) -> SubTile { return x ? st1 : st0; };
+  auto active = [&](int x, int ks) -> bool {
+    const SubTile t = sub(x);
+    if (t.empty()) return false;
+    return !p.causal || (long long)kv_pos0 + ks <= (long long)q_pos0 + t.q_hi - 1;
+  };
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;  // Q_A, then Q_B
+  uint8_t* sKV = smem + 2 * C::Q_BYTES;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_fin, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s[x], 1);
+      mbar_init(&bar_p[x], 128);
+      mbar_init(&bar_o[x], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ========================================================== TMA producer
+    if (lane == 0 && n > 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      const int nq = st1.empty() ? 1 : 2;
+      mbar_arrive_expect_tx(&bar_q, nq * C::Q_BYTES);
+      for (int x = 0; x < nq; ++x)
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, sub(x).h, sub(x).q_lo, b);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      auto push = [&](const CUtensorMap* map, int start) -> bool {
+        if (!pf_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
+        uint8_t* dst = sKV + stage * C::SLAB_BYTES;
+        mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], blk * 64, hk, start, b);
+        ++issued;
+        if (++stage == C::NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        return true;
+      };
+      // first-use order of the MMA: K(0), then per tile V(j), K(j+1)
+      TileWalk kw = walk, vw = walk;
+      int ch, s0, me;
+      kw.next(ch, s0, me);
+      bool ok = push(&mk, s0);
+      for (int j = 0; ok && j < n; ++j) {
+        vw.next(ch, s0, me);
+        ok = push(&mv, s0);
+        if (ok && j + 1 < n) {
+          kw.next(ch, s0, me);
+          ok = push(&mk, s0);
+        }
+      }
+      if (abort_flag) {
+        pf_drain(&bar_q, 0);
+        const int outstanding = issued < C::NST ? issued : C::NST;
+        for (int i = 0; i < outstanding; ++i) {
+          const int pos = issued - 1 - i;
+          pf_drain(&bar_full[pos % C::NST], (uint32_t)((pos / C::NST) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ========================================================== MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
+      constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, D, kBf16, true);
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t skv = smem_u32(sKV);
+      int pv_count[2] = {0, 0};
+      bool ok = pf_wait(&bar_q, 0, &abort_flag, 5);
+      tc_fence_after_sync();
+      // slab s (push order K0 V0 K1 V1 ...) lives in stage s % NST, phase (s / NST) & 1
+      auto wait_slab = [&](int s) -> bool {
+        if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, 2)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      // A wait issued after this thread's own tcgen05.commit stalls until the
+      // committed MMAs are done, draining the tensor pipe.  So waits are
+      // gathered at one point per sub-tile and tile: before PV_x(j), the thread
+      // waits for P_x(j), V(j) and, if S_x(j+1) follows, K(j+1); then it issues
+      // PV_x(j) and S_x(j+1) back to back (16 MMAs) with no wait in between.
+      auto issue_s = [&](int x, int j, bool first, bool last) -> bool {
+        const int slab = 2 * j;
+        if (first && j == 0 && !wait_slab(slab)) return false;
+        const uint32_t kbase = skv + (slab % C::NST) * C::SLAB_BYTES;
+        const uint32_t qbase = sq + x * C::Q_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+          mma_ss(tmem + static_cast<uint32_t>(x * 128), smem_desc_sw128(qbase + off, 16, 1024),
+                 smem_desc_sw128(kbase + off, 16, 1024), kIdescS, ks != 0);
+        }
+        if (last) mma_commit(&bar_empty[slab % C::NST]);
+        mma_commit(&bar_s[x]);
+        return true;
+      };
+      // next_k_first: S_x(j+1) follows and is the first use of K(j+1)
+      auto issue_pv = [&](int x, int j, bool first, bool last, bool next_k_first) -> bool {
+        if (!pf_wait(&bar_p[x], (uint32_t)(pv_count[x] & 1), &abort_flag, 3)) return false;
+        tc_fence_after_sync();
+        const int slab = 2 * j + 1;
+        if (first && !wait_slab(slab)) return false;
+        if (next_k_first && !wait_slab(2 * j + 2)) return false;
+        const uint32_t vbase = skv + (slab % C::NST) * C::SLAB_BYTES;
+        const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
+#pragma unroll
+        for (int ks = 0; ks < C::BN / 16; ++ks)
+          mma_ts(tmem + C::O_COL + static_cast<uint32_t>(x * D), p_tmem + ks * 8,
+                 smem_desc_sw128(vbase + ks * 2048, 16384, 1024), kIdescPV, (pv_count[x] > 0 || ks > 0));
+        if (last) mma_commit(&bar_empty[slab % C::NST]);
+        mma_commit(&bar_o[x]);
+        ++pv_count[x];
+        return true;
+      };
+      TileWalk mw = walk;
+      int ch, kcur, me;
+      mw.next(ch, kcur, me);
+      bool a_cur = active(0, kcur), b_cur = active(1, kcur);
+      if (ok && a_cur) ok = issue_s(0, 0, true, !b_cur);
+      if (ok && b_cur) ok = issue_s(1, 0, !a_cur, true);
+      for (int j = 0; ok && j < n; ++j) {
+        int knext = 0;
+        bool a_nxt = false, b_nxt = false;
+        if (j + 1 < n) {
+          mw.next(ch, knext, me);
+          a_nxt = active(0, knext);
+          b_nxt = active(1, knext);
+        }
+        // K(j+1) is waited for with the first PV that precedes its first use
+        if (a_cur) {
+          ok = issue_pv(0, j, true, !b_cur, a_nxt);
+          if (!ok) break;
+        } else if (a_nxt && !wait_slab(2 * j + 2)) {
+          break;
+        }
+        if (a_nxt) {
+          ok = issue_s(0, j + 1, true, !b_nxt);
+          if (!ok) break;
+        }
+        if (b_cur) {
+          ok = issue_pv(1, j, !a_cur, true, !a_nxt && b_nxt);
+          if (!ok) break;
+        } else if (!a_nxt && b_nxt && !wait_slab(2 * j + 2)) {
+          break;
+        }
+        if (b_nxt) {
+          ok = issue_s(1, j + 1, !a_nxt, true);
+          if (!ok) break;
+        }
+        a_cur = a_nxt;
+        b_cur = b_nxt;
+      }
+      // every MMA issued above must finish before TMEM is released
+      mma_commit(&bar_fin);
+      pf_drain(&bar_fin, 0);
+    }
+  } else {
+    // ========================================================== softmax + epilogue
+    const int x = (warp - 2) >> 2;  // sub-tile of this warpgroup
+    const int wq = warp & 3;        // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const SubTile me_t = sub(x);
+    const int q_row = me_t.q_lo + row;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t scol = lane_addr + static_cast<uint32_t>(x * 128);
+    const uint32_t ocol = lane_addr + C::O_COL + static_cast<uint32_t>(x * D);
+    const float c = p.scale_log2;  // > 0
+    const uint64_t c2 = f2_make(c, c);
+    float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
+    float l_run = 0.f;             // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
+    float lr_run = 0.f;            // sum of the rounded P the MMA multiplies V by: normalises O
+    float m_max = -CUDART_INF_F;   // true running max (partial mode)
+    int cnt = 0;                   // tiles of the walk this sub-tile took part in
+    bool ok = true;
+    TileWalk sw = walk;
+    for (int j = 0; j < n; ++j) {
+      int ch, kstart, mend;
+      sw.next(ch, kstart, mend);
+      if (!active(x, kstart)) continue;
+      if (!pf_wait(&bar_s[x], (uint32_t)(cnt & 1), &abort_flag, 6)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(scol, r0);
+      tmem_ld32(scol + 32, r1);
+      tmem_ld32(scol + 64, r2);
+      tmem_ld32(scol + 96, r3);
+      tmem_ld_wait(r0);
+      tmem_ld_wait(r1);
+      tmem_ld_wait(r2);
+      tmem_ld_wait(r3);
+
+      // mask the diagonal / tail tile: key kstart + i is visible iff i < lim
+      const bool need_mask =
+          (kstart + C::BN > mend) ||
+          (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + me_t.q_lo));
+      if (need_mask) {
+        long long lim = (long long)mend - kstart;
+        if (p.causal) {
+          const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
+          lim = lc < lim ? lc : lim;
+        }
+        const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= lim) r0[i] = ninf;
+          if (i + 32 >= lim) r1[i] = ninf;
+          if (i + 64 >= lim) r2[i] = ninf;
+          if (i + 96 >= lim) r3[i] = ninf;
+        }
+      }
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float a = fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8])),
+                        fmaxf(__uint_as_float(r0[i + 16]), __uint_as_float(r0[i + 24])));
+        float bb = fmaxf(fmaxf(__uint_as_float(r1[i]), __uint_as_float(r1[i + 8])),
+                         fmaxf(__uint_as_float(r1[i + 16]), __uint_as_float(r1[i + 24])));
+        float cc = fmaxf(fmaxf(__uint_as_float(r2[i]), __uint_as_float(r2[i + 8])),
+                         fmaxf(__uint_as_float(r2[i + 16]), __uint_as_float(r2[i + 24])));
+        float dd = fmaxf(fmaxf(__uint_as_float(r3[i]), __uint_as_float(r3[i + 8])),
+                         fmaxf(__uint_as_float(r3[i + 16]), __uint_as_float(r3[i + 24])));
+        mx8[i] = fmaxf(fmaxf(a, bb), fmaxf(cc, dd));
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_tile = mx * c;  // -inf when the whole row is masked
+      if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
+      const float m_new = fmaxf(m_run, m_tile);
+      const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
+      float alpha = 1.f;
+      if (raise) {
+        alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
+        m_run = m_new;
+        l_run *= alpha;
+        lr_run *= alpha;
+      }
+      const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+      const uint64_t nm2 = f2_make(neg_m, neg_m);
+      uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
+      uint32_t pk[16];
+      auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 e = f2_split(f2_fma(f2_make_u(r[2 * i], r[2 * i + 1]), c2, nm2));
+          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+          pk[i] = pack_half2<kBf16>(p0, p1);
+          sum2 = f2_add(sum2, f2_make(p0, p1));
+          // O is normalised by the sum of the rounded weights it was built
+          // from, so O / l is a weighted mean with consistent weights
+          const float2 pr = unpack_half2<kBf16>(pk[i]);
+          sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
+        }
+        tmem_st16(scol + col, pk);
+      };
+      // P overwrites the first 64 columns of S, already in registers
+      pack_chunk(r0, 0);
+      pack_chunk(r1, 16);
+      pack_chunk(r2, 32);
+      pack_chunk(r3, 48);
+      const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
+      l_run += sv.x + sv.y;
+      lr_run += srv.x + srv.y;
+
+      if (cnt > 0) {
+        // the previous PV of this sub-tile must be complete before O is
+        // rescaled (and it keeps the phase bookkeeping of bar_o exact)
+        if (!pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 7)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(ocol + cc * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(ocol + cc * 32, o);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bar_p[x]);
+      ++cnt;
+    }
+    if (ok && cnt > 0) {
+      ok = pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 8);
+      tc_fence_after_sync();
+    }
+    if (ok) {
+      const bool row_valid = q_row < me_t.q_hi;
+      const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + me_t.h;
+      const size_t lse_idx = ((size_t)b * p.h_q + me_t.h) * p.S_q + q_row;
+      constexpr float kLn2 = 0.693147180559945309f;
+      if constexpr (kMode != kModePartial) {
+        const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          if (cnt > 0) {
+            tmem_ld32(ocol + cc * 32, o);
+            tmem_ld_wait(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
+        }
+        if (p.lse != nullptr && row_valid)
+          p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
+      } else {
+        const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
+        const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
+        // O re-weighted so that O / l equals the consistently normalised O_acc / lr
+        const float fo = any ? f * (l_run / lr_run) : 0.f;
+        float* orow = p.o_part + row_idx * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          if (cnt > 0) {
+            tmem_ld32(ocol + cc * 32, o);
+            tmem_ld_wait(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (row_valid) {
+            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
+                                    __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+          }
+        }
+        if (row_valid) {
+          p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
+          p.l_out[lse_idx] = any ? l_run * f : 0.f;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool kBf16, int kMode>
+attn_status_t launch_pair_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
+  using C = PairCfg<D>;
+  auto kern = prefill_pair_kernel<D, kBf16, kMode>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Grid of the paired kernel for a dense / partial launch of `p`.
+inline dim3 pair_grid(const PrefillParams& p) {
+  if (p.pair_heads) return dim3((p.S_q + 127) / 128, p.h_q / 2, p.B);
+  return dim3((p.S_q + 255) / 256, p.h_q, p.B);
+}
+
+template <int D>
+attn_status_t launch_pair_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                   const CUtensorMap& mv, int mode, bool bf16, dim3 grid, cudaStream_t s) {
+  if (bf16) {
+    switch (mode) {
+      case kModeDense: return launch_pair_variant<D, true, kModeDense>(p, mq, mk, mv, grid, s);
+      case kModePartial: return launch_pair_variant<D, true, kModePartial>(p, mq, mk, mv, grid, s);
+      case kModeJagged: return launch_pair_variant<D, true, kModeJagged>(p, mq, mk, mv, grid, s);
+    }
+  } else {
+    switch (mode) {
+      case kModeDense: return launch_pair_variant<D, false, kModeDense>(p, mq, mk, mv, grid, s);
+      case kModePartial: return launch_pair_variant<D, false, kModePartial>(p, mq, mk, mv, grid, s);
+      case kModeJagged: return launch_pair_variant<D, false, kModeJagged>(p, mq, mk, mv, grid, s);
+    }
+  }
+  return ATTN_ERR_INVALID_ARG;
+}
+
+}  // namespace attn

@@ -58,8 +58,9 @@ def gen(shape_q, shape_kv, dtype, seed):
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_prefill_dense_ragged(D, dtype, causal):
-    B, S_, h_q, h_kv = 2, 300, 4, 2
+@pytest.mark.parametrize("S_,h_q,h_kv", [(300, 4, 2), (300, 2, 2), (520, 3, 1)])
+def test_prefill_dense_ragged(D, dtype, causal, S_, h_q, h_kv):
+    B = 2
     q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), dtype, seed=D + causal)
     o = torch.empty_like(q)
     lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
@@ -199,29 +200,32 @@ def _jagged_case(lengths, H, D, seed, causal=True):
     return q, k, v, o, lse, offs, ws
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [True, False])
-def test_jagged_parity_and_worklist(causal):
-    lengths = [0, 1, 5, 127, 128, 129, 300, 1024, 77, 0, 256, 640]
-    H, D = 2, 128
+def test_jagged_parity_and_worklist(causal, D):
+    lengths = [0, 1, 5, 127, 128, 129, 300, 1024, 77, 0, 256, 640, 383, 384, 385]
+    H = 2
     q, k, v, o, lse, offs, ws = _jagged_case(lengths, H, D, seed=21, causal=causal)
     O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), causal)
     close_o(o, O)
     close_lse(lse, L)
-    # worklist: the same items as the oracle's flattened worklist, bit for bit
+    # worklist: the same items as the oracle's flattened worklist, bit for bit.  Head
+    # dims 64/128 run two 128-row sub-tiles per CTA, so their Q tiles are 256 rows.
+    block_m = 256 if D <= 128 else 128
     words = ws.view(torch.int32).cpu().numpy()
     count = int(words[0])
     items = words[4:4 + 4 * count].reshape(count, 4)
-    ref = S.jagged_worklist(offs, 128, 128, causal)
+    ref = S.jagged_worklist(offs, block_m, 128, causal)
     assert count == len(ref)
     got = sorted(map(tuple, items.tolist()))
     want = sorted((it["ordered_begin"], it["range_len"], it["tile_start"], it["tile_extent"]) for it in ref)
     assert got == want
     # order: non-increasing Q-tile count per sequence, and each sequence's tiles last-to-first
-    ntiles = [(r[1] + 127) // 128 for r in items]
+    ntiles = [(r[1] + block_m - 1) // block_m for r in items]
     assert all(a >= b for a, b in zip(ntiles, ntiles[1:]))
     for a, b in zip(items, items[1:]):
         if a[0] == b[0]:
-            assert b[2] == a[2] - 128
+            assert b[2] == a[2] - block_m
 
 
 def test_jagged_random_lengths():
