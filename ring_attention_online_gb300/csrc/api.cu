@@ -55,10 +55,36 @@ constexpr float kLog2e = 1.4426950408889634f;
 bool paired(int D) { return D <= 128; }
 int jagged_block(int D) { return paired(D) ? 2 * ATTN_BLOCK_M : ATTN_BLOCK_M; }
 
-dim3 dense_grid(const PrefillParams& p, int D) {
-  if (!paired(D)) return dim3((p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, p.h_q, p.B);
-  if (p.pair_heads) return dim3((p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, p.h_q / 2, p.B);
-  return dim3((p.S_q + 2 * ATTN_BLOCK_M - 1) / (2 * ATTN_BLOCK_M), p.h_q, p.B);
+// Streaming multiprocessors of the current device (the persistent grid size).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+// Persistent grid: one CTA per SM, or fewer when there are fewer items.
+dim3 persistent_grid(long long items) {
+  const long long g = items < sm_count() ? items : sm_count();
+  return dim3((unsigned)(g > 0 ? g : 1));
+}
+
+// Fills the work-item decomposition of the paired kernel and its grid (one
+// item per CTA); the single-tile kernel takes one CTA per (Q tile, head,
+// batch).  False when the item count does not fit a 32-bit item index.
+bool dense_grid(PrefillParams& p, int D, dim3* grid) {
+  if (!paired(D)) {
+    *grid = dim3((p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, p.h_q, p.B);
+    return true;
+  }
+  const int rows = p.pair_heads ? ATTN_BLOCK_M : 2 * ATTN_BLOCK_M;
+  p.n_qt = (p.S_q + rows - 1) / rows;
+  p.n_y = p.pair_heads ? p.h_q / 2 : p.h_q;
+  const long long items = (long long)p.n_qt * p.n_y * p.B;
+  if (items > 0x7fffffffLL) return false;
+  p.n_items = (int)items;
+  *grid = dim3((unsigned)items);  // one item per CTA: see prefill_pair_kernel.cuh
+  return true;
 }
 
 attn_status_t launch_prefill(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
@@ -126,7 +152,9 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  return launch_prefill(p, mq, mk, mv, kModeDense, bf16, D, dense_grid(p, D), reinterpret_cast<cudaStream_t>(stream));
+  dim3 grid;
+  if (!dense_grid(p, D, &grid)) return ATTN_ERR_UNSUPPORTED;
+  return launch_prefill(p, mq, mk, mv, kModeDense, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o_unnorm,
@@ -160,7 +188,9 @@ attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m
   if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  return launch_prefill(p, mq, mk, mv, kModePartial, bf16, D, dense_grid(p, D), reinterpret_cast<cudaStream_t>(stream));
+  dim3 grid;
+  if (!dense_grid(p, D, &grid)) return ATTN_ERR_UNSUPPORTED;
+  return launch_prefill(p, mq, mk, mv, kModePartial, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, int C, int B, int S_q, int H, int D,
@@ -197,6 +227,7 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
   const int block = jagged_block(D);
   const size_t max_items = jagged_max_items(num_seqs, total_tokens, block);
   if (max_items > 0x7fffffffULL || H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (paired(D) && (unsigned long long)max_items * H > 0x7fffffffULL) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* wl = static_cast<int*>(workspace);
   st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, block, wl, (int)max_items, s);
@@ -221,7 +252,7 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
       !make_map(&mk, k, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  const dim3 grid((unsigned)max_items, H, 1);
+  const dim3 grid = paired(D) ? persistent_grid((long long)max_items * H) : dim3((unsigned)max_items, H, 1);
   return launch_prefill(p, mq, mk, mv, kModeJagged, bf16, D, grid, s);
 }
 

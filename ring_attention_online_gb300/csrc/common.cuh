@@ -34,6 +34,10 @@ struct PrefillParams {
   int B, S_q, S_kv, h_q, h_kv, group;
   int causal, num_chunks;
   int pair_heads;  // paired kernel: the two Q sub-tiles are heads (h, h+1) at one Q tile (else Q tiles 2t, 2t+1)
+  // paired kernel (persistent), dense / partial: n_items = n_qt * n_y * B work
+  // items over n_qt Q tiles (128 rows with pair_heads, else 256) and n_y head
+  // pairs (pair_heads) or heads
+  int n_items, n_qt, n_y;
   int q_pos0, kv_pos0, kv_lo, kv_hi;  // dense / partial key range and positions
   float scale_log2;                   // softmax scale * log2(e)
   // jagged worklist: count followed by items {seq_begin, seq_len, tile_start, tile_extent}

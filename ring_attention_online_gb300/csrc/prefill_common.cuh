@@ -12,16 +12,32 @@ namespace attn {
 
 static __device__ unsigned int g_prefill_status;
 
-// Bounded wait used by every role; also gives up as soon as another CTA of
-// any launch has reported a timeout (so a broken pipeline ends quickly).
+// Bounded wait used by every role; also gives up once another CTA of any
+// launch has reported a timeout, so a broken pipeline ends quickly.  The
+// barrier is polled first: the clock and the device-wide status word (a
+// global-memory round trip) are read only every 512 failed polls, because
+// these waits sit on the critical path between the MMA and softmax roles.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort, uint32_t site) {
-  if (mbar_try_wait(smem_u32(bar), parity)) return true;
-  if (*reinterpret_cast<volatile unsigned int*>(&g_prefill_status) & kStatusTimeout) {
-    *abort = 1u;
-    return false;
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  uint64_t t0 = 0;
+#pragma unroll 1
+  for (uint32_t it = 0;; ++it) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (*abort) return false;
+    if ((it & 15u) == 15u) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      const bool late = now - t0 > kWaitTimeoutNs;
+      if (late) atomicOr(&g_prefill_status, kStatusTimeout | (site << kStatusSiteShift));
+      if (late || (*reinterpret_cast<volatile unsigned int*>(&g_prefill_status) & kStatusTimeout)) {
+        *abort = 1u;
+        return false;
+      }
+    }
   }
-  return mbar_wait_bounded(bar, parity, abort, &g_prefill_status, kStatusTimeout | (site << kStatusSiteShift),
-                           kWaitTimeoutNs);
 }
 
 // Wait used only while tearing down after an abort: ignores the abort flag.

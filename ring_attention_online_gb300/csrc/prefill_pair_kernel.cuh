@@ -16,9 +16,20 @@
 // tiles of one head / sequence and share the walk of the later one, the
 // earlier sub-tile sitting out the tiles it cannot see (no masked-only work).
 //
+// A CTA walks a list of work items (a Q tile pair with its KV walk): the next
+// item's Q and first K/V tiles load, and its first S tiles are computed, while
+// the previous item's last P.V products and epilogue finish.  Jagged launches
+// are persistent (one CTA per SM, items in a snake order over the CTAs, longest
+// first), because their items are short; dense launches run one item per CTA
+// in the hardware's launch order, which keeps the CTAs that run at one time on
+// the K/V of one head (a persistent static split measured 1.65x the DRAM reads
+// of that order on the long GQA workload).
+//
 // CTA layout (320 threads):
-//   warp 0      TMA producer: both Q sub-tiles, then K(0), V(0), K(1), V(1), ...
-//               through a ring of NST stages (one stage = one K or V tile).
+//   warp 0      TMA producer: per item both Q sub-tiles (once the previous
+//               item's MMAs are done with the Q buffer), then K(0), V(0),
+//               K(1), V(1), ... through a ring of NST stages (one stage = one
+//               K or V tile) that runs on across items.
 //   warp 1      TMEM owner (512 columns: S_A, S_B, O_A, O_B) and single-thread
 //               tcgen05 issuer, in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
 //               PV_B(j) S_B(j+1) | ... so one sub-tile's MMAs run while the
@@ -55,6 +66,71 @@ struct SubTile {
   __device__ bool empty() const { return q_hi <= q_lo; }
 };
 
+// One work item of the paired kernel: two sub-tiles and the KV range they walk.
+struct PairItem {
+  int b, kv_lo, kv_hi, q_pos0, kv_pos0;
+  SubTile st0, st1;
+};
+
+// Number of work items of a launch (jagged: read from the device worklist).
+template <int kMode>
+__device__ __forceinline__ int pair_item_count(const PrefillParams& p) {
+  if constexpr (kMode == kModeJagged) return *p.work_count * p.h_q;
+  return p.n_items;
+}
+
+// Item k of the launch.  Dense / partial items: the Q tiles of one head (pair)
+// and batch are consecutive, longest causal walk first, so the CTAs that run
+// at one time share the K/V of one head in L2.  Jagged items follow the
+// worklist (longest sequences first), all heads of one Q tile in a row.
+template <int kMode>
+__device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int k) {
+  constexpr int BM = 128;
+  PairItem it;
+  if constexpr (kMode == kModeJagged) {
+    const int4 w = p.work_items[k / p.h_q];  // a 256-row Q tile of one sequence
+    const int h = k % p.h_q;
+    const int a_hi = w.z + min(w.w, BM);
+    it.b = 0;
+    it.st0 = SubTile{h, w.z, a_hi};
+    it.st1 = SubTile{h, a_hi, w.z + w.w};
+    it.kv_lo = w.x;
+    it.kv_hi = w.x + w.y;  // seq_offsets[seq_idx + 1]
+    it.q_pos0 = 0;
+    it.kv_pos0 = 0;
+  } else {
+    const int yb = k / p.n_qt;
+    const int t_rank = k - yb * p.n_qt;
+    const int y = yb % p.n_y;
+    it.b = yb / p.n_y;
+    const int t = p.causal ? p.n_qt - 1 - t_rank : t_rank;
+    it.kv_lo = p.kv_lo;
+    it.kv_hi = p.kv_hi;
+    it.q_pos0 = p.q_pos0;
+    it.kv_pos0 = p.kv_pos0;
+    if (p.pair_heads) {
+      const int lo = t * BM, hi = min(lo + BM, p.S_q);
+      it.st0 = SubTile{2 * y, lo, hi};
+      it.st1 = SubTile{2 * y + 1, lo, hi};
+    } else {
+      const int lo = t * 2 * BM;
+      const int mid = min(lo + BM, p.S_q), hi = min(lo + 2 * BM, p.S_q);
+      it.st0 = SubTile{y, lo, mid};
+      it.st1 = SubTile{y, mid, hi};
+    }
+  }
+  return it;
+}
+
+// The r-th item of this CTA in the snake order (-1 when there is none).
+__device__ __forceinline__ int pair_item_index(int r, int total) {
+  const int g = (int)gridDim.x;
+  const long long base = (long long)r * g;
+  if (base >= total) return -1;
+  const long long k = base + ((r & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  return k < total ? (int)k : -2;  // -2: none this round, and none later
+}
+
 template <int D, bool kBf16, int kMode>
 // 10 warps put three on two of the four SM sub-partitions (16K registers
 // each), so at most 168 registers per thread
@@ -62,63 +138,17 @@ __global__ void __launch_bounds__(320, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = PairCfg<D>;
+  // dense / partial CTAs take one item; the item loops below then run once
+  // (a loop the compiler cannot bound costs ~5% in the softmax code)
+  constexpr bool kPersistent = kMode == kModeJagged;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_fin;
+  __shared__ uint64_t bar_q, bar_qe, bar_fin;
   __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
   __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
 
-  // ------------------------------------------------------------ work item
-  int b, kv_lo, kv_hi, q_pos0, kv_pos0;
-  SubTile st0, st1;
-  if constexpr (kMode == kModeJagged) {
-    const int item = blockIdx.x;
-    if (item >= *p.work_count) return;  // the grid is an upper bound on the item count
-    const int4 it = p.work_items[item];  // a 256-row Q tile of one sequence
-    b = 0;
-    const int h = blockIdx.y;
-    const int a_hi = it.z + min(it.w, C::BM);
-    st0 = SubTile{h, it.z, a_hi};
-    st1 = SubTile{h, a_hi, it.z + it.w};
-    kv_lo = it.x;
-    kv_hi = it.x + it.y;  // seq_offsets[seq_idx + 1]
-    q_pos0 = 0;
-    kv_pos0 = 0;
-  } else {
-    b = blockIdx.z;
-    kv_lo = p.kv_lo;
-    kv_hi = p.kv_hi;
-    q_pos0 = p.q_pos0;
-    kv_pos0 = p.kv_pos0;
-    // causal: longest Q tiles first, so the short ones fill the tail
-    const int t = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-    if (p.pair_heads) {
-      const int lo = t * C::BM, hi = min(lo + C::BM, p.S_q);
-      st0 = SubTile{2 * (int)blockIdx.y, lo, hi};
-      st1 = SubTile{2 * (int)blockIdx.y + 1, lo, hi};
-    } else {
-      const int lo = t * 2 * C::BM;
-      const int mid = min(lo + C::BM, p.S_q), hi = min(lo + 2 * C::BM, p.S_q);
-      st0 = SubTile{(int)blockIdx.y, lo, mid};
-      st1 = SubTile{(int)blockIdx.y, mid, hi};
-    }
-  }
-  const int hk = st0.h / p.group;
-  const int u_lo = st0.q_lo;
-  const int u_hi = st1.empty() ? st0.q_hi : max(st0.q_hi, st1.q_hi);
-  TileWalk walk;
-  walk.init(u_lo, u_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, p.num_chunks, C::BN);
-  const int n = walk.count();
-  // sub-tile x takes part in the tile starting at key `ks` iff it has rows and
-  // (causal) its last query sees the tile's first key
-  auto sub = [&](int x) -> SubTile { return x ? st1 : st0; };
-  auto active = [&](int x, int ks) -> bool {
-    const SubTile t = sub(x);
-    if (t.empty()) return false;
-    return !p.causal || (long long)kv_pos0 + ks <= (long long)q_pos0 + t.q_hi - 1;
-  };
-
+  const int total = pair_item_count<kMode>(p);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;  // Q_A, then Q_B
   uint8_t* sKV = smem + 2 * C::Q_BYTES;
@@ -128,6 +158,7 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_qe, 1);
     mbar_init(&bar_fin, 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -149,21 +180,33 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
 
+  // Per item, every role derives the same walk.  Sub-tile x takes part in the
+  // tile starting at key `ks` iff it has rows and (causal) its last query
+  // sees the tile's first key.
+  auto item_walk = [&](const PairItem& it, TileWalk& walk) -> int {
+    const int u_lo = it.st0.q_lo;
+    const int u_hi = it.st1.empty() ? it.st0.q_hi : max(it.st0.q_hi, it.st1.q_hi);
+    walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, p.num_chunks, C::BN);
+    return walk.count();
+  };
+  auto active = [&](const PairItem& it, int x, int ks) -> bool {
+    const SubTile t = x ? it.st1 : it.st0;
+    if (t.empty()) return false;
+    return !p.causal || (long long)it.kv_pos0 + ks <= (long long)it.q_pos0 + t.q_hi - 1;
+  };
+
   if (warp == 0) {
     // ========================================================== TMA producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
-      const int nq = st1.empty() ? 1 : 2;
-      mbar_arrive_expect_tx(&bar_q, nq * C::Q_BYTES);
-      for (int x = 0; x < nq; ++x)
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, sub(x).h, sub(x).q_lo, b);
       int stage = 0;
       uint32_t phase = 0;
-      int issued = 0;
-      auto push = [&](const CUtensorMap* map, int start) -> bool {
+      int issued = 0;   // K/V slabs issued so far (all items)
+      int q_loads = 0;  // items whose Q was loaded
+      bool ok = true;
+      auto push = [&](const CUtensorMap* map, int hk, int start, int b) -> bool {
         if (!pf_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
         uint8_t* dst = sKV + stage * C::SLAB_BYTES;
         mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
@@ -176,21 +219,42 @@ __global__ void __launch_bounds__(320, 1)
         }
         return true;
       };
-      // first-use order of the MMA: K(0), then per tile V(j), K(j+1)
-      TileWalk kw = walk, vw = walk;
-      int ch, s0, me;
-      kw.next(ch, s0, me);
-      bool ok = push(&mk, s0);
-      for (int j = 0; ok && j < n; ++j) {
-        vw.next(ch, s0, me);
-        ok = push(&mv, s0);
-        if (ok && j + 1 < n) {
-          kw.next(ch, s0, me);
-          ok = push(&mk, s0);
+      for (int r = 0; ok && (kPersistent || r == 0); ++r) {
+        const int k = pair_item_index(r, total);
+        if (k < 0) break;
+        const PairItem it = pair_item<kMode>(p, k);
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        const int hk = it.st0.h / p.group;
+        // Q once the previous item's MMAs are done with the Q buffer, then
+        // K/V in the MMA's first-use order: K(0), and per tile V(j), K(j+1)
+        TileWalk kw = walk, vw = walk;
+        int ch, s0, me;
+        if (q_loads > 0 && !pf_wait(&bar_qe, (uint32_t)((q_loads - 1) & 1), &abort_flag, 4)) break;
+        const int nq = it.st1.empty() ? 1 : 2;
+        mbar_arrive_expect_tx(&bar_q, nq * C::Q_BYTES);
+        for (int x = 0; x < nq; ++x) {
+          const SubTile t = x ? it.st1 : it.st0;
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, t.h, t.q_lo, it.b);
+        }
+        ++q_loads;
+        kw.next(ch, s0, me);
+        ok = push(&mk, hk, s0, it.b);
+        if (!ok) break;
+        for (int j = 0; ok && j < n; ++j) {
+          vw.next(ch, s0, me);
+          ok = push(&mv, hk, s0, it.b);
+          if (ok && j + 1 < n) {
+            kw.next(ch, s0, me);
+            ok = push(&mk, hk, s0, it.b);
+          }
         }
       }
       if (abort_flag) {
-        pf_drain(&bar_q, 0);
+        // copies may still be landing in shared memory: wait for them
+        if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
         const int outstanding = issued < C::NST ? issued : C::NST;
         for (int i = 0; i < outstanding; ++i) {
           const int pos = issued - 1 - i;
@@ -200,95 +264,118 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 1) {
     // ========================================================== MMA issuer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, D, kBf16, true);
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
-      int pv_count[2] = {0, 0};
-      bool ok = pf_wait(&bar_q, 0, &abort_flag, 5);
-      tc_fence_after_sync();
-      // slab s (push order K0 V0 K1 V1 ...) lives in stage s % NST, phase (s / NST) & 1
+      int pv_count[2] = {0, 0};  // P.V groups issued per sub-tile (all items)
+      int slab0 = 0;             // first K/V slab of the current item
+      int q_items = 0;           // items whose Q was consumed
+      bool ok = true;
+      // slab s (push order K0 V0 K1 V1 ... over all items) lives in stage
+      // s % NST, phase (s / NST) & 1
       auto wait_slab = [&](int s) -> bool {
         if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, 2)) return false;
         tc_fence_after_sync();
         return true;
       };
-      // A wait issued after this thread's own tcgen05.commit stalls until the
-      // committed MMAs are done, draining the tensor pipe.  So waits are
-      // gathered at one point per sub-tile and tile: before PV_x(j), the thread
-      // waits for P_x(j), V(j) and, if S_x(j+1) follows, K(j+1); then it issues
-      // PV_x(j) and S_x(j+1) back to back (16 MMAs) with no wait in between.
-      auto issue_s = [&](int x, int j, bool first, bool last) -> bool {
-        const int slab = 2 * j;
-        if (first && j == 0 && !wait_slab(slab)) return false;
-        const uint32_t kbase = skv + (slab % C::NST) * C::SLAB_BYTES;
-        const uint32_t qbase = sq + x * C::Q_BYTES;
+      // A wait issued after this thread's own tcgen05 work stalls until that
+      // work has drained from the tensor pipe.  So waits are gathered at one
+      // point per sub-tile and tile: before PV_x(j), the thread waits for
+      // P_x(j), V(j) and, if S_x(j+1) follows, K(j+1); then it issues PV_x(j)
+      // and S_x(j+1) back to back (16 MMAs) with no wait in between.
+      auto issue_s = [&](int x, int slab, bool wait_k, bool last) -> bool {
+        if (wait_k && !wait_slab(slab)) return false;
+        const uint64_t kdesc = smem_desc_sw128(skv + (slab % C::NST) * C::SLAB_BYTES, 16, 1024);
+        const uint64_t qdesc = smem_desc_sw128(sq + x * C::Q_BYTES, 16, 1024);
+        const uint32_t s_tmem = tmem + static_cast<uint32_t>(x * 128);
+        // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle row,
+        // the next 64-column block every four steps
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-          mma_ss(tmem + static_cast<uint32_t>(x * 128), smem_desc_sw128(qbase + off, 16, 1024),
-                 smem_desc_sw128(kbase + off, 16, 1024), kIdescS, ks != 0);
+          mma_ss(s_tmem, desc_advance(qdesc, off), desc_advance(kdesc, off), kIdescS, ks != 0);
         }
         if (last) mma_commit(&bar_empty[slab % C::NST]);
         mma_commit(&bar_s[x]);
         return true;
       };
-      // next_k_first: S_x(j+1) follows and is the first use of K(j+1)
-      auto issue_pv = [&](int x, int j, bool first, bool last, bool next_k_first) -> bool {
+      // first_v: the first use of V(j); next_k: K(j+1) is first used by the
+      // S MMA that follows
+      auto issue_pv = [&](int x, int slab, bool first_v, bool last, bool next_k, bool acc) -> bool {
         if (!pf_wait(&bar_p[x], (uint32_t)(pv_count[x] & 1), &abort_flag, 3)) return false;
         tc_fence_after_sync();
-        const int slab = 2 * j + 1;
-        if (first && !wait_slab(slab)) return false;
-        if (next_k_first && !wait_slab(2 * j + 2)) return false;
-        const uint32_t vbase = skv + (slab % C::NST) * C::SLAB_BYTES;
+        if (first_v && !wait_slab(slab)) return false;
+        if (next_k && !wait_slab(slab + 1)) return false;
+        const uint64_t vdesc = smem_desc_sw128(skv + (slab % C::NST) * C::SLAB_BYTES, 16384, 1024);
         const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
+        const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(x * D);
+        // 16 keys of V (16 rows of 256 bytes, two swizzle atoms) per MMA
 #pragma unroll
         for (int ks = 0; ks < C::BN / 16; ++ks)
-          mma_ts(tmem + C::O_COL + static_cast<uint32_t>(x * D), p_tmem + ks * 8,
-                 smem_desc_sw128(vbase + ks * 2048, 16384, 1024), kIdescPV, (pv_count[x] > 0 || ks > 0));
+          mma_ts(o_tmem, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV, (ks > 0 || acc) ? 1u : 0u);
         if (last) mma_commit(&bar_empty[slab % C::NST]);
         mma_commit(&bar_o[x]);
         ++pv_count[x];
         return true;
       };
-      TileWalk mw = walk;
-      int ch, kcur, me;
-      mw.next(ch, kcur, me);
-      bool a_cur = active(0, kcur), b_cur = active(1, kcur);
-      if (ok && a_cur) ok = issue_s(0, 0, true, !b_cur);
-      if (ok && b_cur) ok = issue_s(1, 0, !a_cur, true);
-      for (int j = 0; ok && j < n; ++j) {
-        int knext = 0;
-        bool a_nxt = false, b_nxt = false;
-        if (j + 1 < n) {
-          mw.next(ch, knext, me);
-          a_nxt = active(0, knext);
-          b_nxt = active(1, knext);
+      for (int r = 0; ok && (kPersistent || r == 0); ++r) {
+        const int k = pair_item_index(r, total);
+        if (k < 0) break;
+        const PairItem it = pair_item<kMode>(p, k);
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        if (!pf_wait(&bar_q, (uint32_t)(q_items & 1), &abort_flag, 5)) break;
+        tc_fence_after_sync();
+        ++q_items;
+        bool acc[2] = {false, false};  // O_x already holds this item's sum
+        int ch, kcur, me;
+        walk.next(ch, kcur, me);
+        bool a_cur = active(it, 0, kcur), b_cur = active(it, 1, kcur);
+        if (a_cur && !issue_s(0, slab0, true, !b_cur)) break;
+        if (b_cur && !issue_s(1, slab0, !a_cur, true)) break;
+        // the Q buffer is free once the item's last S MMA has run
+        for (int j = 0; ok && j < n; ++j) {
+          const int sv = slab0 + 2 * j + 1;  // V(j); K(j+1) is sv + 1
+          int knext = 0;
+          bool a_nxt = false, b_nxt = false;
+          if (j + 1 < n) {
+            walk.next(ch, knext, me);
+            a_nxt = active(it, 0, knext);
+            b_nxt = active(it, 1, knext);
+          }
+          if (a_cur) {
+            ok = issue_pv(0, sv, true, !b_cur, a_nxt, acc[0]);
+            acc[0] = true;
+            if (!ok) break;
+          } else if (a_nxt && !wait_slab(sv + 1)) {
+            ok = false;
+            break;
+          }
+          if (a_nxt && !issue_s(0, sv + 1, false, !b_nxt)) {
+            ok = false;
+            break;
+          }
+          if (b_cur) {
+            ok = issue_pv(1, sv, !a_cur, true, !a_nxt && b_nxt, acc[1]);
+            acc[1] = true;
+            if (!ok) break;
+          } else if (!a_nxt && b_nxt && !wait_slab(sv + 1)) {
+            ok = false;
+            break;
+          }
+          if (b_nxt && !issue_s(1, sv + 1, false, true)) {
+            ok = false;
+            break;
+          }
+          a_cur = a_nxt;
+          b_cur = b_nxt;
         }
-        // K(j+1) is waited for with the first PV that precedes its first use
-        if (a_cur) {
-          ok = issue_pv(0, j, true, !b_cur, a_nxt);
-          if (!ok) break;
-        } else if (a_nxt && !wait_slab(2 * j + 2)) {
-          break;
-        }
-        if (a_nxt) {
-          ok = issue_s(0, j + 1, true, !b_nxt);
-          if (!ok) break;
-        }
-        if (b_cur) {
-          ok = issue_pv(1, j, !a_cur, true, !a_nxt && b_nxt);
-          if (!ok) break;
-        } else if (!a_nxt && b_nxt && !wait_slab(2 * j + 2)) {
-          break;
-        }
-        if (b_nxt) {
-          ok = issue_s(1, j + 1, !a_nxt, true);
-          if (!ok) break;
-        }
-        a_cur = a_nxt;
-        b_cur = b_nxt;
+        // the item's MMAs, the last readers of its Q, release the Q buffer
+        mma_commit(&bar_qe);
+        slab0 += 2 * n;
       }
       // every MMA issued above must finish before TMEM is released
       mma_commit(&bar_fin);
@@ -299,120 +386,125 @@ __global__ void __launch_bounds__(320, 1)
     const int x = (warp - 2) >> 2;  // sub-tile of this warpgroup
     const int wq = warp & 3;        // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
-    const SubTile me_t = sub(x);
-    const int q_row = me_t.q_lo + row;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t scol = lane_addr + static_cast<uint32_t>(x * 128);
     const uint32_t ocol = lane_addr + C::O_COL + static_cast<uint32_t>(x * D);
     const float c = p.scale_log2;  // > 0
     const uint64_t c2 = f2_make(c, c);
-    float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
-    float l_run = 0.f;             // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
-    float lr_run = 0.f;            // sum of the rounded P the MMA multiplies V by: normalises O
-    float m_max = -CUDART_INF_F;   // true running max (partial mode)
-    int cnt = 0;                   // tiles of the walk this sub-tile took part in
+    const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
+    int cnt = 0;  // tiles this sub-tile took part in (all items) = its P.V groups
     bool ok = true;
-    TileWalk sw = walk;
-    for (int j = 0; j < n; ++j) {
-      int ch, kstart, mend;
-      sw.next(ch, kstart, mend);
-      if (!active(x, kstart)) continue;
-      if (!pf_wait(&bar_s[x], (uint32_t)(cnt & 1), &abort_flag, 6)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(scol, r0);
-      tmem_ld32(scol + 32, r1);
-      tmem_ld32(scol + 64, r2);
-      tmem_ld32(scol + 96, r3);
-      tmem_ld_wait(r0);
-      tmem_ld_wait(r1);
-      tmem_ld_wait(r2);
-      tmem_ld_wait(r3);
-
-      // mask the diagonal / tail tile: key kstart + i is visible iff i < lim
-      const bool need_mask =
-          (kstart + C::BN > mend) ||
-          (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + me_t.q_lo));
-      if (need_mask) {
-        long long lim = (long long)mend - kstart;
-        if (p.causal) {
-          const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
-          lim = lc < lim ? lc : lim;
-        }
-        const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (i >= lim) r0[i] = ninf;
-          if (i + 32 >= lim) r1[i] = ninf;
-          if (i + 64 >= lim) r2[i] = ninf;
-          if (i + 96 >= lim) r3[i] = ninf;
-        }
-      }
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float a = fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8])),
-                        fmaxf(__uint_as_float(r0[i + 16]), __uint_as_float(r0[i + 24])));
-        float bb = fmaxf(fmaxf(__uint_as_float(r1[i]), __uint_as_float(r1[i + 8])),
-                         fmaxf(__uint_as_float(r1[i + 16]), __uint_as_float(r1[i + 24])));
-        float cc = fmaxf(fmaxf(__uint_as_float(r2[i]), __uint_as_float(r2[i + 8])),
-                         fmaxf(__uint_as_float(r2[i + 16]), __uint_as_float(r2[i + 24])));
-        float dd = fmaxf(fmaxf(__uint_as_float(r3[i]), __uint_as_float(r3[i + 8])),
-                         fmaxf(__uint_as_float(r3[i + 16]), __uint_as_float(r3[i + 24])));
-        mx8[i] = fmaxf(fmaxf(a, bb), fmaxf(cc, dd));
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_tile = mx * c;  // -inf when the whole row is masked
-      if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
-      const float m_new = fmaxf(m_run, m_tile);
-      const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
-      float alpha = 1.f;
-      if (raise) {
-        alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
-        m_run = m_new;
-        l_run *= alpha;
-        lr_run *= alpha;
-      }
-      const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
-      const uint64_t nm2 = f2_make(neg_m, neg_m);
-      uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
-      uint32_t pk[16];
-      auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 e = f2_split(f2_fma(f2_make_u(r[2 * i], r[2 * i + 1]), c2, nm2));
-          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
-          pk[i] = pack_half2<kBf16>(p0, p1);
-          sum2 = f2_add(sum2, f2_make(p0, p1));
-          // O is normalised by the sum of the rounded weights it was built
-          // from, so O / l is a weighted mean with consistent weights
-          const float2 pr = unpack_half2<kBf16>(pk[i]);
-          sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
-        }
-        tmem_st16(scol + col, pk);
-      };
-      // P overwrites the first 64 columns of S, already in registers
-      pack_chunk(r0, 0);
-      pack_chunk(r1, 16);
-      pack_chunk(r2, 32);
-      pack_chunk(r3, 48);
-      const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
-      l_run += sv.x + sv.y;
-      lr_run += srv.x + srv.y;
-
-      if (cnt > 0) {
-        // the previous PV of this sub-tile must be complete before O is
-        // rescaled (and it keeps the phase bookkeeping of bar_o exact)
-        if (!pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 7)) {
+    for (int r = 0; ok && (kPersistent || r == 0); ++r) {
+      const int k = pair_item_index(r, total);
+      if (k < 0) break;
+      const PairItem it = pair_item<kMode>(p, k);
+      TileWalk walk;
+      const int n = item_walk(it, walk);
+      const SubTile me_t = x ? it.st1 : it.st0;
+      const int q_row = me_t.q_lo + row;
+      float m_run = -CUDART_INF_F;  // reference max (exp2 domain), raised lazily
+      float l_run = 0.f;            // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
+      float lr_run = 0.f;           // sum of the rounded P the MMA multiplies V by: normalises O
+      float m_max = -CUDART_INF_F;  // true running max (partial mode)
+      int cnt_item = 0;             // tiles of this item this sub-tile took part in
+      for (int j = 0; j < n; ++j) {
+        int ch, kstart, mend;
+        walk.next(ch, kstart, mend);
+        if (!active(it, x, kstart)) continue;
+        if (!pf_wait(&bar_s[x], (uint32_t)(cnt & 1), &abort_flag, 6)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, raise)) {
+        // S_x(j) was issued after this sub-tile's previous P.V by the same
+        // thread, so its completion also means that P.V has finished: O may
+        // be rescaled without waiting on bar_o.
+        const bool need_mask =
+            (kstart + C::BN > mend) ||
+            (p.causal && ((long long)it.kv_pos0 + kstart + C::BN - 1 > (long long)it.q_pos0 + me_t.q_lo));
+        long long lim = C::BN;  // key kstart + i is visible iff i < lim
+        if (need_mask) {
+          lim = (long long)mend - kstart;
+          if (p.causal) {
+            const long long lc = (long long)it.q_pos0 + q_row - it.kv_pos0 - kstart + 1;
+            lim = lc < lim ? lc : lim;
+          }
+        }
+        // the first 64 columns are reduced while the second pair of loads is in flight
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(scol, r0);
+        tmem_ld32(scol + 32, r1);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        tmem_ld32(scol + 64, r2);
+        tmem_ld32(scol + 96, r3);
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i >= lim) r0[i] = ninf;
+            if (i + 32 >= lim) r1[i] = ninf;
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mx8[i] = fmax3(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8]), __uint_as_float(r0[i + 16]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r0[i + 24]), __uint_as_float(r1[i]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 8]), __uint_as_float(r1[i + 16]));
+        }
+        tmem_ld_wait(r2);
+        tmem_ld_wait(r3);
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i + 64 >= lim) r2[i] = ninf;
+            if (i + 96 >= lim) r3[i] = ninf;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 24]), __uint_as_float(r2[i]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r2[i + 8]), __uint_as_float(r2[i + 16]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r2[i + 24]), __uint_as_float(r3[i]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r3[i + 8]), __uint_as_float(r3[i + 16]));
+          mx8[i] = fmaxf(mx8[i], __uint_as_float(r3[i + 24]));
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        const float m_tile = mx * c;  // -inf when the whole row is masked
+        if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
+        float alpha = 1.f;
+        if (raise) {
+          alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
+          m_run = m_new;
+          l_run *= alpha;
+          lr_run *= alpha;
+        }
+        const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+        const uint64_t nm2 = f2_make(neg_m, neg_m);
+        uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
+        uint32_t pk[16];
+        auto pack_chunk = [&](uint32_t (&rr)[32], uint32_t col) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 e = f2_split(f2_fma(f2_make_u(rr[2 * i], rr[2 * i + 1]), c2, nm2));
+            const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+            pk[i] = pack_half2<kBf16>(p0, p1);
+            sum2 = f2_add(sum2, f2_make(p0, p1));
+            // O is normalised by the sum of the rounded weights it was built
+            // from, so O / l is a weighted mean with consistent weights
+            const float2 pr = unpack_half2<kBf16>(pk[i]);
+            sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
+          }
+          tmem_st16(scol + col, pk);
+        };
+        // P overwrites the first 64 columns of S, already in registers
+        pack_chunk(r0, 0);
+        pack_chunk(r1, 16);
+        // O (complete up to the previous tile, see above) is rescaled before
+        // P(j) is published
+        if (cnt_item > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
@@ -423,20 +515,26 @@ __global__ void __launch_bounds__(320, 1)
             tmem_st32(ocol + cc * 32, o);
           }
         }
+        pack_chunk(r2, 32);
+        pack_chunk(r3, 48);
+        const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
+        l_run += sv.x + sv.y;
+        lr_run += srv.x + srv.y;
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bar_p[x]);
+        ++cnt;
+        ++cnt_item;
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&bar_p[x]);
-      ++cnt;
-    }
-    if (ok && cnt > 0) {
-      ok = pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 8);
-      tc_fence_after_sync();
-    }
-    if (ok) {
+      if (!ok) break;
+      if (cnt_item > 0) {
+        // the item's last P.V of this sub-tile (earlier ones are done, see above)
+        if (!pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 8)) break;
+        tc_fence_after_sync();
+      }
       const bool row_valid = q_row < me_t.q_hi;
-      const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + me_t.h;
-      const size_t lse_idx = ((size_t)b * p.h_q + me_t.h) * p.S_q + q_row;
+      const size_t row_idx = ((size_t)it.b * p.S_q + q_row) * p.h_q + me_t.h;
+      const size_t lse_idx = ((size_t)it.b * p.h_q + me_t.h) * p.S_q + q_row;
       constexpr float kLn2 = 0.693147180559945309f;
       if constexpr (kMode != kModePartial) {
         const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
@@ -444,7 +542,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
-          if (cnt > 0) {
+          if (cnt_item > 0) {
             tmem_ld32(ocol + cc * 32, o);
             tmem_ld_wait(o);
           } else {
@@ -472,7 +570,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
-          if (cnt > 0) {
+          if (cnt_item > 0) {
             tmem_ld32(ocol + cc * 32, o);
             tmem_ld_wait(o);
           } else {
@@ -513,12 +611,6 @@ attn_status_t launch_pair_variant(const PrefillParams& p, const CUtensorMap& mq,
     return ATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
-// Grid of the paired kernel for a dense / partial launch of `p`.
-inline dim3 pair_grid(const PrefillParams& p) {
-  if (p.pair_heads) return dim3((p.S_q + 127) / 128, p.h_q / 2, p.B);
-  return dim3((p.S_q + 255) / 256, p.h_q, p.B);
 }
 
 template <int D>

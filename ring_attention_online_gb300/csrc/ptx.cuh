@@ -236,6 +236,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The descriptor of the operand `bytes` further on in shared memory (a
+// multiple of 16).  The start address is the low field and operands sit in
+// the 228 KB window, so the add cannot carry out of it: one 32-bit add.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  const uint32_t lo = static_cast<uint32_t>(desc) + (bytes >> 4);
+  return (desc & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation.
 // A and B share the input type (fp16 or bf16).  b_mn_major selects an
 // N-contiguous B operand (V in P.V); A is always K-major.
@@ -253,6 +261,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // Two fp32 values rounded to nearest-even 16-bit floats, packed lo | hi << 16.
