@@ -12,13 +12,13 @@
 //    at min(kv_end, tile_q.end) (no fully masked tile is visited); only the
 //    diagonal and tail tiles are masked.
 //
-// CTA layout (320 threads):
+// CTA layout (352 threads):
 //   warp 0      TMA producer: Q tile once, then K/V 128-column slabs through a
-//               ring of NST shared-memory stages, in the order the MMA needs.
-//   warp 1      TMEM owner and single-thread tcgen05 issuer:
-//               S(0), then per tile j: S(j+1), PV(j).  S(j) = Q.K_j^T goes to one
-//               of two 128-column TMEM buffers; PV(j) reads P(j) (bf16/fp16,
-//               written over S(j) by the softmax warps) as the TMEM A operand.
+//               ring of NST shared-memory stages: K(0), then per tile K(j+1), V(j).
+//   warp 1      TMEM owner and S issuer: S(j) = Q.K_j^T into one of two
+//               128-column TMEM buffers, once PV(j-2) has read that buffer.
+//   warp 10     PV issuer: O += P(j).V_j, P(j) (bf16/fp16, written over S(j) by
+//               the softmax warps) being the TMEM A operand.
 //   warps 2..9  softmax + epilogue: each query row (TMEM lane) is shared by two
 //               warps, one per half of the tile's 128 keys and of O's columns.
 //               Scores are scaled into the exp2 domain; the running max is
@@ -54,7 +54,7 @@ struct PrefillCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   // S(j) / P(j) live in TMEM columns [128*(j%2), 128*(j%2)+128); O after them
   static constexpr uint32_t O_COL = 256;
-  static constexpr int THREADS = 320;  // TMA warp, MMA warp, 8 softmax warps
+  static constexpr int THREADS = 352;  // TMA warp, S issuer, 8 softmax warps, PV issuer
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(NST >= 2, "at least two K/V stages");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
@@ -62,12 +62,13 @@ struct PrefillCfg {
 };
 
 template <int D, bool kBf16, int kMode>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = PrefillCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_o, bar_fin;
+  __shared__ uint64_t bar_q, bar_fin;
+  __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2]
   __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
   __shared__ uint64_t bar_s[2], bar_p[2];
   __shared__ uint32_t tmem_slot;
@@ -117,8 +118,9 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
-    mbar_init(&bar_o, 1);
-    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_o[0], 1);
+    mbar_init(&bar_o[1], 1);
+    mbar_init(&bar_fin, 2);  // one commit per MMA issuer
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
@@ -190,69 +192,82 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ========================================================== MMA issuer
+  } else if (warp == 1 || warp == 10) {
+    // ========================================================== MMA issuers
+    // Warp 1 issues S(j), warp 10 issues PV(j).  A thread's wait stalls until
+    // the tcgen05 work it issued itself has drained from the tensor pipe, so
+    // with one issuer every wait (for P, or for a K/V stage) emptied the pipe.
+    // Split by kind, each issuer only waits on work of the other roles: the S
+    // issuer on K stages and on PV(j-2) (S(j) overwrites P(j-2) in its TMEM
+    // buffer, and MMAs of different threads are not ordered), the PV issuer on
+    // P(j) and V stages.
     if (lane == 0 && n > 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, C::SC, kBf16, true);
-      const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
-      int stage = 0;
-      uint32_t phase = 0;
-      auto advance = [&]() {
-        if (++stage == C::NST) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      };
-      auto issue_s = [&](int j) -> bool {
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+      // stage order of the producer: K(0), then per tile K(j+1), V(j); in
+      // tiles of NH slabs, K(j) is tile 2j - 1 (j > 0) and V(j) tile 2j + 2,
+      // except V(n - 1), the last tile, 2n - 1
+      auto k_tile = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
+      auto v_tile = [&](int j) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; };
+      auto wait_slabs = [&](int tile, uint32_t site) -> bool {
         for (int hs = 0; hs < C::NH; ++hs) {
-          if (!pf_wait(&bar_full[stage], phase, &abort_flag, 2)) return false;
-          tc_fence_after_sync();
-          const uint32_t kbase = skv + stage * C::SLAB_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < C::SC / 16; ++ks) {
-            const uint32_t qoff = (hs * C::BLK_PER_SLAB + ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-            const uint32_t koff = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-            mma_ss(d_tmem, smem_desc_sw128(sq + qoff, 16, 1024), smem_desc_sw128(kbase + koff, 16, 1024), kIdescS,
-                   (hs | ks) != 0);
-          }
-          mma_commit(&bar_empty[stage]);
-          advance();
+          const int s = tile * C::NH + hs;
+          if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, site)) return false;
         }
-        mma_commit(&bar_s[j & 1]);
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        if (!pf_wait(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3)) return false;
         tc_fence_after_sync();
-        const uint32_t p_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
-        for (int hs = 0; hs < C::NH; ++hs) {
-          if (!pf_wait(&bar_full[stage], phase, &abort_flag, 4)) return false;
-          tc_fence_after_sync();
-          const uint32_t vbase = skv + stage * C::SLAB_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < C::BN / 16; ++ks)
-            mma_ts(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, smem_desc_sw128(vbase + ks * 2048, 16384, 1024),
-                   kIdescPV, (j > 0 || ks > 0));
-          mma_commit(&bar_empty[stage]);
-          advance();
-        }
-        mma_commit(&bar_o);
         return true;
       };
-      bool ok = pf_wait(&bar_q, 0, &abort_flag, 5);
-      tc_fence_after_sync();
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          ok = issue_s(j + 1);
+      bool ok = true;
+      if (warp == 1) {
+        const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        ok = pf_wait(&bar_q, 0, &abort_flag, 5);
+        tc_fence_after_sync();
+        for (int j = 0; ok && j < n; ++j) {
+          if (j >= 2) {
+            ok = pf_wait(&bar_o[j & 1], (uint32_t)(((j - 2) >> 1) & 1), &abort_flag, 11);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          const int kt = k_tile(j);
+          ok = wait_slabs(kt, 2);
           if (!ok) break;
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+          for (int hs = 0; hs < C::NH; ++hs) {
+            const int stage = (kt * C::NH + hs) % C::NST;
+            const uint64_t kdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < C::SC / 16; ++ks) {
+              const uint32_t qoff = (hs * C::BLK_PER_SLAB + ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+              const uint32_t koff = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+              mma_ss(d_tmem, desc_advance(qdesc, qoff), desc_advance(kdesc, koff), kIdescS, (hs | ks) != 0);
+            }
+            mma_commit(&bar_empty[stage]);
+          }
+          mma_commit(&bar_s[j & 1]);
         }
-        ok = issue_pv(j);
+      } else {
+        for (int j = 0; ok && j < n; ++j) {
+          ok = pf_wait(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3);
+          if (!ok) break;
+          const int vt = v_tile(j);
+          ok = wait_slabs(vt, 4);
+          if (!ok) break;
+          const uint32_t p_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
+          for (int hs = 0; hs < C::NH; ++hs) {
+            const int stage = (vt * C::NH + hs) % C::NST;
+            const uint64_t vdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16384, 1024);
+#pragma unroll
+            for (int ks = 0; ks < C::BN / 16; ++ks)
+              mma_ts(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                     ks > 0 ? 1u : acc0);
+            mma_commit(&bar_empty[stage]);
+          }
+          mma_commit(&bar_o[j & 1]);
+        }
       }
-      // every MMA issued above must finish before TMEM is released
+      // every MMA either issuer issued must finish before TMEM is released
       mma_commit(&bar_fin);
       pf_drain(&bar_fin, 0);
     }
@@ -312,13 +327,13 @@ __global__ void __launch_bounds__(320, 1)
       }
       float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        mx8[i] = fmaxf(fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8])),
-                             fmaxf(__uint_as_float(r0[i + 16]), __uint_as_float(r0[i + 24]))),
-                       fmaxf(fmaxf(__uint_as_float(r1[i]), __uint_as_float(r1[i + 8])),
-                             fmaxf(__uint_as_float(r1[i + 16]), __uint_as_float(r1[i + 24]))));
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int i = 0; i < 8; ++i) {
+        mx8[i] = fmax3(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8]), __uint_as_float(r0[i + 16]));
+        mx8[i] = fmax3(mx8[i], __uint_as_float(r0[i + 24]), __uint_as_float(r1[i]));
+        mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 8]), __uint_as_float(r1[i + 16]));
+        mx8[i] = fmaxf(mx8[i], __uint_as_float(r1[i + 24]));
+      }
+      float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       // both halves of the row see each other's max (the S(j) columns are all in
       // registers by now, so P may overwrite them after this barrier)
       xch_max[buf][half][row] = mx;
@@ -362,25 +377,25 @@ __global__ void __launch_bounds__(320, 1)
       l_run += (sa[0] + sa[1]) + (sa[2] + sa[3]);
       lr_run += (sr[0] + sr[1]) + (sr[2] + sr[3]);
 
-      if (j > 0) {
-        // PV(j-1) must be complete before O is rescaled (and it keeps the
-        // phase bookkeeping of bar_o exact)
-        if (!pf_wait(&bar_o, (uint32_t)((j - 1) & 1), &abort_flag, 7)) {
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        // PV(j-1) must be complete before O is rescaled.  PV(j-2) is (S(j) was
+        // issued after it), so with P.V groups alternating between two
+        // barriers this wait is never more than one phase behind, and the
+        // tiles that need no rescale need not wait at all.
+        if (!pf_wait(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 7)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-          for (int cc = 0; cc < HD / 32; ++cc) {
-            uint32_t o[32];
-            const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
-            tmem_ld32(oa, o);
-            tmem_ld_wait(o);
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          uint32_t o[32];
+          const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
+          tmem_ld32(oa, o);
+          tmem_ld_wait(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(oa, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(oa, o);
         }
       }
       tmem_st_wait();
@@ -388,7 +403,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(&bar_p[buf]);
     }
     if (ok && n > 0) {
-      ok = pf_wait(&bar_o, (uint32_t)((n - 1) & 1), &abort_flag, 8);
+      // the last P.V (the earlier ones are done or finish before it)
+      ok = pf_wait(&bar_o[(n - 1) & 1], (uint32_t)(((n - 1) >> 1) & 1), &abort_flag, 8);
       tc_fence_after_sync();
     }
     // the row's sums are split over the two halves
