@@ -355,27 +355,29 @@ __global__ void __launch_bounds__(352, 1)
         lr_run *= alpha;
       }
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sr[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
+      uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
       uint32_t pk[16];
       auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * i]), c, neg_m));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * i + 1]), c, neg_m));
+          const float2 e = f2_split(f2_fma(f2_make_u(r[2 * i], r[2 * i + 1]), c2, nm2));
+          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
           pk[i] = pack_half2<kBf16>(p0, p1);
-          sa[i & 3] += p0 + p1;
+          sum2 = f2_add(sum2, f2_make(p0, p1));
           // O is normalised by the sum of the rounded weights it was built
           // from, so O / l is a weighted mean with consistent weights
           const float2 pr = unpack_half2<kBf16>(pk[i]);
-          sr[i & 3] += pr.x + pr.y;
+          sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
         }
         tmem_st16(scol + col, pk);
       };
       // P(j) for keys [64*half, 64*half+64) goes to columns [32*half, 32*half+32)
       pack_chunk(r0, half * 32);
       pack_chunk(r1, half * 32 + 16);
-      l_run += (sa[0] + sa[1]) + (sa[2] + sa[3]);
-      lr_run += (sr[0] + sr[1]) + (sr[2] + sr[3]);
+      const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
+      l_run += sv.x + sv.y;
+      lr_run += srv.x + srv.y;
 
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
         // PV(j-1) must be complete before O is rescaled.  PV(j-2) is (S(j) was
