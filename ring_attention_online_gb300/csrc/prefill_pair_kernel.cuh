@@ -25,17 +25,18 @@
 // the K/V of one head (a persistent static split measured 1.65x the DRAM reads
 // of that order on the long GQA workload).
 //
-// CTA layout (320 threads):
+// CTA layout (352 threads):
 //   warp 0      TMA producer: per item both Q sub-tiles (once the previous
 //               item's MMAs are done with the Q buffer), then K(0), V(0),
 //               K(1), V(1), ... through a ring of NST stages (one stage = one
 //               K or V tile) that runs on across items.
-//   warp 1      TMEM owner (512 columns: S_A, S_B, O_A, O_B) and single-thread
-//               tcgen05 issuer, in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
-//               PV_B(j) S_B(j+1) | ... so one sub-tile's MMAs run while the
-//               other sub-tile's softmax is computed.
+//   warp 1      TMEM owner (512 columns: S_A, S_B, O_A, O_B) and S issuer:
+//               S_A(j), S_B(j) per tile, each once its sub-tile's previous
+//               P.V has read the P held in its S buffer.
 //   warps 2..5  softmax + epilogue of sub-tile A, one query row per thread.
 //   warps 6..9  the same for sub-tile B.
+//   warp 10     P.V issuer: PV_A(j), PV_B(j) as each P becomes ready, so one
+//               sub-tile's MMAs run while the other sub-tile's softmax runs.
 // P(j) of a sub-tile (bf16/fp16) overwrites the first 64 columns of its S
 // buffer and is the TMEM A operand of P.V.  Every wait is bounded.
 #pragma once
@@ -55,7 +56,7 @@ struct PairCfg {
   static constexpr int SMEM_BYTES = 2 * Q_BYTES + NST * SLAB_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;  // S_A 0..127, S_B 128..255, O_A 256.., O_B 256+D..
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
   static_assert(D == 64 || D == 128, "paired kernel: head dim 64 or 128");
   static_assert(NST >= 3, "K(j+1) must be loadable while K(j) and V(j) are held");
   static_assert(SMEM_BYTES <= 227 * 1024 - 512, "shared memory budget");
@@ -132,9 +133,9 @@ __device__ __forceinline__ int pair_item_index(int r, int total) {
 }
 
 template <int D, bool kBf16, int kMode>
-// 10 warps put three on two of the four SM sub-partitions (16K registers
+// 11 warps put three on three of the four SM sub-partitions (16K registers
 // each), so at most 168 registers per thread
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = PairCfg<D>;
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(320, 1)
     abort_flag = 0;
     mbar_init(&bar_q, 1);
     mbar_init(&bar_qe, 1);
-    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_fin, 2);  // one commit per MMA issuer
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
@@ -262,62 +263,29 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ========================================================== MMA issuer
+  } else if (warp == 1 || warp == 10) {
+    // ========================================================== MMA issuers
+    // Warp 1 issues the S MMAs, warp 10 the P.V MMAs.  A thread's wait stalls
+    // until the tcgen05 work it issued itself has drained from the tensor
+    // pipe, so each issuer only waits on the other roles: the S issuer on K
+    // stages and, because S_x overwrites the sub-tile's previous P_x in its
+    // TMEM buffer and MMAs of different threads are not ordered, on that
+    // previous P.V; the P.V issuer on P_x and V stages.
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, D, kBf16, true);
       const uint32_t sq = smem_u32(sQ);
       const uint32_t skv = smem_u32(sKV);
-      int pv_count[2] = {0, 0};  // P.V groups issued per sub-tile (all items)
-      int slab0 = 0;             // first K/V slab of the current item
-      int q_items = 0;           // items whose Q was consumed
+      const bool s_role = warp == 1;
+      int groups[2] = {0, 0};  // S (or P.V) groups issued per sub-tile so far, all items
+      int slab0 = 0;           // first K/V slab of the current item
+      int q_items = 0;         // items whose Q was consumed
       bool ok = true;
       // slab s (push order K0 V0 K1 V1 ... over all items) lives in stage
       // s % NST, phase (s / NST) & 1
       auto wait_slab = [&](int s) -> bool {
         if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, 2)) return false;
         tc_fence_after_sync();
-        return true;
-      };
-      // A wait issued after this thread's own tcgen05 work stalls until that
-      // work has drained from the tensor pipe.  So waits are gathered at one
-      // point per sub-tile and tile: before PV_x(j), the thread waits for
-      // P_x(j), V(j) and, if S_x(j+1) follows, K(j+1); then it issues PV_x(j)
-      // and S_x(j+1) back to back (16 MMAs) with no wait in between.
-      auto issue_s = [&](int x, int slab, bool wait_k, bool last) -> bool {
-        if (wait_k && !wait_slab(slab)) return false;
-        const uint64_t kdesc = smem_desc_sw128(skv + (slab % C::NST) * C::SLAB_BYTES, 16, 1024);
-        const uint64_t qdesc = smem_desc_sw128(sq + x * C::Q_BYTES, 16, 1024);
-        const uint32_t s_tmem = tmem + static_cast<uint32_t>(x * 128);
-        // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle row,
-        // the next 64-column block every four steps
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-          mma_ss(s_tmem, desc_advance(qdesc, off), desc_advance(kdesc, off), kIdescS, ks != 0);
-        }
-        if (last) mma_commit(&bar_empty[slab % C::NST]);
-        mma_commit(&bar_s[x]);
-        return true;
-      };
-      // first_v: the first use of V(j); next_k: K(j+1) is first used by the
-      // S MMA that follows
-      auto issue_pv = [&](int x, int slab, bool first_v, bool last, bool next_k, bool acc) -> bool {
-        if (!pf_wait(&bar_p[x], (uint32_t)(pv_count[x] & 1), &abort_flag, 3)) return false;
-        tc_fence_after_sync();
-        if (first_v && !wait_slab(slab)) return false;
-        if (next_k && !wait_slab(slab + 1)) return false;
-        const uint64_t vdesc = smem_desc_sw128(skv + (slab % C::NST) * C::SLAB_BYTES, 16384, 1024);
-        const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
-        const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(x * D);
-        // 16 keys of V (16 rows of 256 bytes, two swizzle atoms) per MMA
-#pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks)
-          mma_ts(o_tmem, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV, (ks > 0 || acc) ? 1u : 0u);
-        if (last) mma_commit(&bar_empty[slab % C::NST]);
-        mma_commit(&bar_o[x]);
-        ++pv_count[x];
         return true;
       };
       for (int r = 0; ok && (kPersistent || r == 0); ++r) {
@@ -327,57 +295,68 @@ __global__ void __launch_bounds__(320, 1)
         TileWalk walk;
         const int n = item_walk(it, walk);
         if (n == 0) continue;
-        if (!pf_wait(&bar_q, (uint32_t)(q_items & 1), &abort_flag, 5)) break;
-        tc_fence_after_sync();
-        ++q_items;
-        bool acc[2] = {false, false};  // O_x already holds this item's sum
-        int ch, kcur, me;
-        walk.next(ch, kcur, me);
-        bool a_cur = active(it, 0, kcur), b_cur = active(it, 1, kcur);
-        if (a_cur && !issue_s(0, slab0, true, !b_cur)) break;
-        if (b_cur && !issue_s(1, slab0, !a_cur, true)) break;
-        // the Q buffer is free once the item's last S MMA has run
-        for (int j = 0; ok && j < n; ++j) {
-          const int sv = slab0 + 2 * j + 1;  // V(j); K(j+1) is sv + 1
-          int knext = 0;
-          bool a_nxt = false, b_nxt = false;
-          if (j + 1 < n) {
-            walk.next(ch, knext, me);
-            a_nxt = active(it, 0, knext);
-            b_nxt = active(it, 1, knext);
-          }
-          if (a_cur) {
-            ok = issue_pv(0, sv, true, !b_cur, a_nxt, acc[0]);
-            acc[0] = true;
-            if (!ok) break;
-          } else if (a_nxt && !wait_slab(sv + 1)) {
-            ok = false;
-            break;
-          }
-          if (a_nxt && !issue_s(0, sv + 1, false, !b_nxt)) {
-            ok = false;
-            break;
-          }
-          if (b_cur) {
-            ok = issue_pv(1, sv, !a_cur, true, !a_nxt && b_nxt, acc[1]);
-            acc[1] = true;
-            if (!ok) break;
-          } else if (!a_nxt && b_nxt && !wait_slab(sv + 1)) {
-            ok = false;
-            break;
-          }
-          if (b_nxt && !issue_s(1, sv + 1, false, true)) {
-            ok = false;
-            break;
-          }
-          a_cur = a_nxt;
-          b_cur = b_nxt;
+        if (s_role) {
+          if (!pf_wait(&bar_q, (uint32_t)(q_items & 1), &abort_flag, 5)) break;
+          tc_fence_after_sync();
+          ++q_items;
         }
-        // the item's MMAs, the last readers of its Q, release the Q buffer
-        mma_commit(&bar_qe);
+        bool acc[2] = {false, false};  // O_x already holds this item's sum
+        for (int j = 0; ok && j < n; ++j) {
+          int ch, kstart, me;
+          walk.next(ch, kstart, me);
+          const bool act[2] = {active(it, 0, kstart), active(it, 1, kstart)};
+          const int slab = slab0 + 2 * j + (s_role ? 0 : 1);  // K(j) or V(j)
+          ok = wait_slab(slab);
+          if (!ok) break;
+          const uint32_t stage_addr = skv + (slab % C::NST) * C::SLAB_BYTES;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (!act[x]) continue;
+            const bool last = x == 1 || !act[1];  // last reader of the stage
+            if (s_role) {
+              if (groups[x] > 0) {
+                // the sub-tile's previous P.V has read its P
+                ok = pf_wait(&bar_o[x], (uint32_t)((groups[x] - 1) & 1), &abort_flag, 11);
+                if (!ok) break;
+                tc_fence_after_sync();
+              }
+              const uint64_t kdesc = smem_desc_sw128(stage_addr, 16, 1024);
+              const uint64_t qdesc = smem_desc_sw128(sq + x * C::Q_BYTES, 16, 1024);
+              const uint32_t s_tmem = tmem + static_cast<uint32_t>(x * 128);
+              // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle
+              // row, the next 64-column block every four steps
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+                mma_ss(s_tmem, desc_advance(qdesc, off), desc_advance(kdesc, off), kIdescS, ks != 0);
+              }
+              if (last) mma_commit(&bar_empty[slab % C::NST]);
+              mma_commit(&bar_s[x]);
+            } else {
+              ok = pf_wait(&bar_p[x], (uint32_t)(groups[x] & 1), &abort_flag, 3);
+              if (!ok) break;
+              tc_fence_after_sync();
+              const uint64_t vdesc = smem_desc_sw128(stage_addr, 16384, 1024);
+              const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
+              const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(x * D);
+              // 16 keys of V (16 rows of 256 bytes, two swizzle atoms) per MMA
+#pragma unroll
+              for (int ks = 0; ks < C::BN / 16; ++ks)
+                mma_ts(o_tmem, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                       (ks > 0 || acc[x]) ? 1u : 0u);
+              acc[x] = true;
+              if (last) mma_commit(&bar_empty[slab % C::NST]);
+              mma_commit(&bar_o[x]);
+            }
+            ++groups[x];
+          }
+        }
+        if (!ok) break;
+        // the item's S MMAs, the last readers of its Q, release the Q buffer
+        if (s_role) mma_commit(&bar_qe);
         slab0 += 2 * n;
       }
-      // every MMA issued above must finish before TMEM is released
+      // every MMA either issuer issued must finish before TMEM is released
       mma_commit(&bar_fin);
       pf_drain(&bar_fin, 0);
     }
