@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=HEADLINE, help="workload to report as the line (default: headline)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch / sequence count (smaller cases for profiling)")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override a prefill workload's sequence length (smaller cases for profiling)")
     return ap.parse_args(argv)
 
 
@@ -159,7 +161,7 @@ def causal_pairs(L: int) -> int:
     return L * (L + 1) // 2
 
 
-def make_workload(name: str, device, batch=None):
+def make_workload(name: str, device, batch=None, seq=None):
     """Inputs in HBM plus a step closure for one workload of the pages."""
     import torch
 
@@ -168,6 +170,8 @@ def make_workload(name: str, device, batch=None):
     cfg = dict(syn.WORKLOADS[name])
     if batch is not None:
         cfg["num_seqs" if cfg["kind"] == "jagged" else "B"] = batch
+    if seq is not None and cfg["kind"] == "prefill":
+        cfg["S_q"] = cfg["S_kv"] = seq
     w = {"name": name, "cfg": cfg}
     if cfg["kind"] == "prefill":
         q, k, v = syn.prefill_inputs(cfg, seed=0, device=device)
@@ -205,8 +209,11 @@ def make_workload(name: str, device, batch=None):
         def step(stream=None):
             ra.attn_jagged(q, k, v, o, offs_d, max_len, ws, lse, causal=True, stream=stream)
         flops = 4.0 * cfg["D"] * cfg["H"] * float(sum(causal_pairs(int(L)) for L in lens))
+        # Q, K, V read and O written once, plus the LSE: at 169 FLOP per byte this
+        # workload sits below GB300's ridge point, so HBM is its binding roofline
+        hbm_bytes = 4.0 * T * cfg["H"] * cfg["D"] * 2 + cfg["H"] * T * 4.0
         w.update(step=step, units=flops / 1e12, unit="TFLOP/s", bound="tensor", launches=2, tensors=(q, k, v, o),
-                 kernel_units=flops / 1e12,
+                 kernel_units=flops / 1e12, hbm_bytes=hbm_bytes,
                  config={"workload": name, "num_seqs": cfg["num_seqs"], "total_tokens": T, "H": cfg["H"],
                          "D": cfg["D"], "len_range": [cfg["len_lo"], cfg["len_hi"]], "causal": True,
                          "l2": "inputs larger than L2 (no flush)"})
@@ -349,7 +356,7 @@ def run_ours(args):
     K, W = args.steps, max(args.warmup, 3)
 
     # ---- headline (or the workload named on the command line)
-    w = make_workload(args.workload, device, args.batch)
+    w = make_workload(args.workload, device, args.batch, args.seq)
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     clocks = ClockSampler(int(visible[local]) if len(visible) > local and visible[local].isdigit() else local)
     for _ in range(W):
@@ -367,11 +374,11 @@ def run_ours(args):
     kernel_ms = ms / K  # the dominant kernel's share of a step
     if "merge_only" in w:  # decode: subtract the live-timed merge kernel to get the partial kernel
         kernel_ms = max(kernel_ms - time_steps(w["merge_only"], K, 2, device) / K, 1e-6)
-    traffic = _profiled_traffic(args.workload) if args.batch is None else None
+    traffic = _profiled_traffic(args.workload) if args.batch is None and args.seq is None else None
     line = {"metric": METRIC, "value": round(value, 2), "unit": w["unit"], "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": round(value / world / PAGES_DENSE_CAUSAL_TFS, 3) if args.workload == HEADLINE and
-            args.batch is None else None, "dtype": "bf16", "data": "synthetic",
+            args.batch is None and args.seq is None else None, "dtype": "bf16", "data": "synthetic",
             "config": dict(w["config"], parallelism=f"replicas{world}" if world > 1 else "single"),
             "roofline": roofline(w, kernel_ms, peaks, peak_kind, traffic),
             "gpu_launches": K * w["launches"],
@@ -395,7 +402,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
 
     # ---- secondary workloads (same rules: inputs in HBM, CUDA events, max over ranks)
-    if not args.no_secondary and args.workload == HEADLINE and args.batch is None:
+    if not args.no_secondary and args.workload == HEADLINE and args.batch is None and args.seq is None:
         sec = []
         for name in ("jagged_causal_1152seq_h4_d128", "long_gqa_ring8_s32768_hq64_hkv8_d128",
                      "decode_splitkv_b8_hq64_hkv8_d128_kv1m"):
@@ -412,6 +419,11 @@ def run_ours(args):
                      "roofline": roofline(w, kernel_ms, peaks, peak_kind, _profiled_traffic(name))}
             if "merge_only" in w:
                 entry["merge_ms"] = round(ms_merge, 4)
+            if "hbm_bytes" in w:  # the memory roofline of the same launches
+                gbs = w["hbm_bytes"] / 1e9 / (kernel_ms / 1e3)
+                entry["roofline_hbm"] = {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"],
+                                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                         "bytes_per_step": w["hbm_bytes"], "peak_source": peak_kind}
             sec.append(entry)
             line["gpu_launches"] += k2 * w["launches"]
             status = ra.attn_last_device_status()
