@@ -224,22 +224,14 @@ def make_workload(name: str, device, batch=None, seq=None):
         lse = torch.empty(B, h_q, device=device, dtype=torch.float32)
         ws = torch.empty(ra.attn_decode_workspace_bytes(B, h_q, D, C), dtype=torch.uint8, device=device)
         rows = C * B * h_q
-        f = ws.view(torch.float32)
-        wm, wl = f[:rows].view(C, B, h_q, 1), f[rows:2 * rows].view(C, B, h_q, 1)
-        off = ((rows * 8 + 15) // 16) * 4
-        wo = f[off:off + rows * D].view(C, B, 1, h_q, D)
-        o_merge = torch.empty(B, 1, h_q, D, device=device, dtype=q.dtype)
 
-        def step(stream=None):
+        def step(stream=None):  # one kernel: partials, and the fused merge in each group's last CTA
             ra.attn_decode_splitkv(q, k, v, o, ws, lse, num_splits=C, stream=stream)
-
-        def merge_only(stream=None):
-            ra.attn_merge(wm, wl, wo, o_merge, None, stream=stream)
         kv_bytes = 2.0 * B * S_kv * h_kv * D * 2
         part_bytes = rows * (D + 2) * 4.0
         alg_bytes = kv_bytes + q.numel() * 2 + part_bytes
-        w.update(step=step, units=kv_bytes / 1e9, unit="GB/s", bound="hbm", launches=2, tensors=(q, k, v, o, ws),
-                 merge_only=merge_only, kernel_units=alg_bytes / 1e9,
+        w.update(step=step, units=kv_bytes / 1e9, unit="GB/s", bound="hbm", launches=1, tensors=(q, k, v, o, ws),
+                 kernel_units=alg_bytes / 1e9,
                  config={"workload": name, "B": B, "h_q": h_q, "h_kv": h_kv, "D": D, "S_kv": S_kv,
                          "num_splits": C, "l2": "inputs larger than L2 (no flush)",
                          "unit_note": "K+V bytes read once per step"})
@@ -372,8 +364,6 @@ def run_ours(args):
         raise RuntimeError(f"device status {ra.STATUS.get(status)} after the headline run")
     value = units / (ms_max / 1e3)
     kernel_ms = ms / K  # the dominant kernel's share of a step
-    if "merge_only" in w:  # decode: subtract the live-timed merge kernel to get the partial kernel
-        kernel_ms = max(kernel_ms - time_steps(w["merge_only"], K, 2, device) / K, 1e-6)
     traffic = _profiled_traffic(args.workload) if args.batch is None and args.seq is None else None
     line = {"metric": METRIC, "value": round(value, 2), "unit": w["unit"], "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(ms_max / K, 4), "higher_is_better": True, "scaling": "weak",
@@ -411,14 +401,9 @@ def run_ours(args):
             ms2 = time_steps(w["step"], k2, W, device)
             units2, ms2_max = aggregate(w["units"] * k2, ms2, world, device)
             kernel_ms = ms2 / k2
-            if "merge_only" in w:  # decode: subtract the live-timed merge kernel to get the partial kernel
-                ms_merge = time_steps(w["merge_only"], k2, 2, device) / k2
-                kernel_ms = max(kernel_ms - ms_merge, 1e-6)
             entry = {"workload": name, "value": round(units2 / (ms2_max / 1e3), 2), "unit": w["unit"],
                      "ms_per_step": round(ms2_max / k2, 4), "steps": k2, "config": w["config"],
                      "roofline": roofline(w, kernel_ms, peaks, peak_kind, _profiled_traffic(name))}
-            if "merge_only" in w:
-                entry["merge_ms"] = round(ms_merge, 4)
             if "hbm_bytes" in w:  # the memory roofline of the same launches
                 gbs = w["hbm_bytes"] / 1e9 / (kernel_ms / 1e3)
                 entry["roofline_hbm"] = {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"],

@@ -151,9 +151,13 @@ size_t attn_jagged_workspace_bytes(int num_seqs, int total_tokens, int max_seqle
  *
  * The KV sequence is cut into num_splits chunks of ceil(S_kv / num_splits) keys
  * (trailing chunks may be empty: identity triplets).  One kernel computes a
- * partial (m, l, o) per (batch, query head, chunk) into `workspace`, a second
- * kernel merges them (as attn_merge).  Workspace layout (fp32, contiguous):
- *   m [num_splits,B,h_q], l [num_splits,B,h_q], o [num_splits,B,h_q,D].
+ * partial (m, l, o) per (batch, query head, chunk) into `workspace`; the last CTA
+ * to finish among the num_splits of a (batch, KV head) merges that group's
+ * partials (as attn_merge) into o and lse in the same kernel.  Workspace layout:
+ *   m [num_splits,B,h_q] fp32, l [num_splits,B,h_q] fp32 (16-byte aligned),
+ *   o [num_splits,B,h_q,D] fp32, then B*h_q int32 counters (the call zeroes the
+ *   first B*h_kv on `stream` before its kernel; size them with
+ *   attn_decode_workspace_bytes).
  *   q [B,h_q,D]; k/v [B,S_kv,h_kv,D]; o [B,h_q,D]; lse [B,h_q] fp32 or NULL.
  *   D in {64,128,256}; h_q / h_kv <= 16.
  */
@@ -178,7 +182,7 @@ size_t attn_decode_workspace_bytes(int B, int h_q, int D, int num_splits);
  * The first call on a device looks up the array's device address (with that device
  * current); make that first call before any stream capture.  All calls share the
  * array and it keeps the last call's contents (every entry a call reads is written
- * by that call first); calls whose kernels overlap on the GPU race on it.
+ * or zeroed by that call first); calls whose kernels overlap on the GPU race on it.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,

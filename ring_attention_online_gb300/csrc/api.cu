@@ -260,7 +260,8 @@ size_t attn_decode_workspace_bytes(int B, int h_q, int D, int num_splits) {
   if (B < 0 || h_q < 0 || D < 0 || num_splits < 0) return 0;
   const size_t rows = (size_t)num_splits * B * h_q;
   const size_t ml = (rows * 2 * sizeof(float) + 15) & ~size_t(15);
-  return ml + rows * D * sizeof(float);
+  const size_t counters = ((size_t)B * h_q * sizeof(int) + 15) & ~size_t(15);  // B * h_kv <= B * h_q used
+  return ml + rows * D * sizeof(float) + counters;
 }
 
 attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -280,12 +281,14 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, v
   float* wm = static_cast<float*>(workspace);
   float* wl = wm + rows;
   float* wo = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((rows * 2 * sizeof(float) + 15) & ~size_t(15)));
+  int* counters = reinterpret_cast<int*>(wo + rows * D);
   CUtensorMap mk, mv;
   if (!make_map(&mk, k, bf16, D, h_kv, S_kv, B, 64) || !make_map(&mv, v, bf16, D, h_kv, S_kv, B, 64))
     return ATTN_ERR_CUDA;
-  st = launch_decode_partial(q, mk, mv, wm, wl, wo, B, S_kv, h_q, h_kv, D, bf16, scale * kLog2e, num_splits, s);
-  if (st != ATTN_OK) return st;
-  return launch_merge(wm, wl, wo, num_splits, B, 1, h_q, D, o, bf16, lse, s);
+  // the fused merge counts the chunks of each (batch, KV head) from zero
+  if (cudaMemsetAsync(counters, 0, (size_t)B * h_kv * sizeof(int), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  return launch_decode_partial(q, mk, mv, wm, wl, wo, B, S_kv, h_q, h_kv, D, bf16, scale * kLog2e, num_splits,
+                               counters, o, lse, s);
 }
 
 attn_status_t attn_last_device_status(attn_stream_t stream) {

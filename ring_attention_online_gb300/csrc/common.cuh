@@ -67,10 +67,11 @@ attn_status_t launch_worklist(const int32_t* seq_offsets, int num_seqs, int tota
 unsigned int worklist_take_status(cudaStream_t s);
 attn_status_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t s);
 
-// Split-KV decode partials.
+// Split-KV decode partials; with `counters` (B * h_kv zeroed ints) the last
+// CTA of each (batch, KV head) also merges the partials into `out` and `lse`.
 attn_status_t launch_decode_partial(const void* q, const CUtensorMap& mk, const CUtensorMap& mv, float* m, float* l,
                                     float* o, int B, int S_kv, int h_q, int h_kv, int D, bool bf16, float scale_log2,
-                                    int num_splits, cudaStream_t s);
+                                    int num_splits, int* counters, void* out, float* lse, cudaStream_t s);
 unsigned int decode_take_status(cudaStream_t s);
 
 }  // namespace attn

@@ -15,9 +15,15 @@
 // O += P.V run on mma.sync m16n8k16 with the G query heads as the M rows
 // (padded to 16); the S accumulator fragment is reused as the A fragment of
 // P.V.  At the end the four warps' triplets are merged in shared memory.
+//
+// Fused merge (when `counters` is given): each CTA counts itself in its
+// (batch, KV head) counter after its partials are written, and the last of the
+// num_splits CTAs folds all chunks' partials of its G query heads into the
+// final O and LSE, so no second kernel and no host round trip is needed.
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -100,11 +106,13 @@ __global__ void __launch_bounds__(160) decode_partial_kernel(const __grid_consta
                                                              const uint16_t* __restrict__ q, float* __restrict__ m_out,
                                                              float* __restrict__ l_out, float* __restrict__ o_out,
                                                              int B, int S_kv, int h_q, int h_kv, float c,
-                                                             int num_splits) {
+                                                             int num_splits, int* __restrict__ counters,
+                                                             void* __restrict__ out, float* __restrict__ lse) {
   using C = DecodeCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
   __shared__ uint32_t abort_flag;
+  __shared__ int last_of_group;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int g = blockIdx.x;      // KV head (fastest: the heads of one token row are read together)
@@ -332,33 +340,54 @@ __global__ void __launch_bounds__(160) decode_partial_kernel(const __grid_consta
     }
   }
   (void)ok;
+  if (counters == nullptr) return;
+
+  // ============================================================ fused merge
+  __threadfence();  // this CTA's partials are visible device-wide before it is counted
+  __syncthreads();
+  int* counter = counters + (size_t)b * h_kv + g;
+  if (threadIdx.x == 0) last_of_group = atomicAdd(counter, 1) == num_splits - 1;
+  __syncthreads();
+  if (!last_of_group) return;
+  __threadfence();  // the partials of the CTAs counted before this one are visible
+  const size_t ml_stride = (size_t)B * h_q;
+  for (int r = warp; r < G; r += C::CONSUMERS + 1) {
+    const size_t hrow = (size_t)b * h_q + (size_t)g * G + r;  // [B, h_q]: O is [B, h_q, D]
+    merge_row<D, kBf16>(m_out, l_out, o_out, num_splits, ml_stride, hrow, ml_stride * D, hrow * D, out, lse, hrow,
+                        lane);
+  }
+  if (threadIdx.x == 0) *counter = 0;  // ready for the next call on this workspace
 }
 
 template <int D, bool kBf16>
 static attn_status_t launch_decode_t(const void* q, const CUtensorMap& mk, const CUtensorMap& mv, float* m, float* l,
                                      float* o, int B, int S_kv, int h_q, int h_kv, float c, int num_splits,
-                                     cudaStream_t s) {
+                                     int* counters, void* out, float* lse, cudaStream_t s) {
   using C = DecodeCfg<D>;
   auto kern = decode_partial_kernel<D, kBf16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const dim3 grid(h_kv, num_splits, B);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mk, mv, static_cast<const uint16_t*>(q), m, l, o, B, S_kv, h_q, h_kv,
-                                                c, num_splits);
+                                                c, num_splits, counters, out, lse);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t launch_decode_partial(const void* q, const CUtensorMap& mk, const CUtensorMap& mv, float* m, float* l,
                                     float* o, int B, int S_kv, int h_q, int h_kv, int D, bool bf16, float scale_log2,
-                                    int num_splits, cudaStream_t s) {
+                                    int num_splits, int* counters, void* out, float* lse, cudaStream_t s) {
+#define ATTN_DECODE_CASE(DD)                                                                                     \
+  case DD:                                                                                                       \
+    return bf16 ? launch_decode_t<DD, true>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits,     \
+                                            counters, out, lse, s)                                               \
+                : launch_decode_t<DD, false>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits,    \
+                                             counters, out, lse, s);
   switch (D) {
-    case 64: return bf16 ? launch_decode_t<64, true>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits, s)
-                         : launch_decode_t<64, false>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits, s);
-    case 128: return bf16 ? launch_decode_t<128, true>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits, s)
-                          : launch_decode_t<128, false>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits, s);
-    case 256: return bf16 ? launch_decode_t<256, true>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits, s)
-                          : launch_decode_t<256, false>(q, mk, mv, m, l, o, B, S_kv, h_q, h_kv, scale_log2, num_splits, s);
+    ATTN_DECODE_CASE(64)
+    ATTN_DECODE_CASE(128)
+    ATTN_DECODE_CASE(256)
   }
+#undef ATTN_DECODE_CASE
   return ATTN_ERR_UNSUPPORTED;
 }
 

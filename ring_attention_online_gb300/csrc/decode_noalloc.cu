@@ -11,9 +11,10 @@
 // process exits, and no call here allocates or frees anything.
 //
 // The array is shared by every call on a device and keeps whatever the last
-// call wrote.  Nothing needs to start at zero: the partial kernel writes every
-// (chunk, batch, head) triplet before the merge kernel reads it.  Two calls
-// whose kernels overlap on the GPU (e.g. on two streams) race on the array.
+// call wrote.  Nothing needs to start at zero: each call zeroes its merge
+// counters and writes every (chunk, batch, head) triplet before reading it.
+// Two calls whose kernels overlap on the GPU (e.g. on two streams) race on the
+// array.
 #include <mutex>
 
 #include "common.cuh"

@@ -84,7 +84,8 @@ def test_partial_merge_jagged_decode_validation(lib):
     assert lib.attn_jagged(FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, 1000, 600, 4, 128, 1, 0.1, 1, FAKE, ws,
                            None) == 0
     wd = lib.attn_decode_workspace_bytes(8, 64, 128, 64)
-    assert wd == ((64 * 8 * 64 * 2 * 4 + 15) // 16) * 16 + 64 * 8 * 64 * 128 * 4
+    # m, l (16-byte aligned), O partials, then B * h_q int32 merge counters (16-byte aligned)
+    assert wd == ((64 * 8 * 64 * 2 * 4 + 15) // 16) * 16 + 64 * 8 * 64 * 128 * 4 + ((8 * 64 * 4 + 15) // 16) * 16
     assert lib.attn_decode_splitkv(FAKE, FAKE, FAKE, FAKE, None, 8, 1000, 64, 2, 128, 1, 0.1, 4, FAKE, wd,
                                    None) == 2  # G = 32 > 16
     assert lib.attn_decode_splitkv(FAKE, FAKE, FAKE, FAKE, None, 8, 1000, 64, 8, 128, 1, 0.1, 0, FAKE, wd,

@@ -276,6 +276,27 @@ def test_decode_parity_and_partials(D, h_q, h_kv, S_kv, splits):
     assert np.abs(norm - ref_norm).max() <= TOL_MAX
 
 
+def test_decode_fused_merge_from_a_dirty_workspace_twice():
+    """The group counters of the fused merge are zeroed by each call and left at zero."""
+    B, h_q, h_kv, D, S_kv, splits = 3, 16, 2, 128, 3000, 9
+    q, k, v = syn.qkv((B, h_q, D), (B, S_kv, h_kv, D), "bf16", 77, "cuda")
+    scale = 1 / math.sqrt(D)
+    nbytes = ra.attn_decode_workspace_bytes(B, h_q, D, splits)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")  # stale counters, NaN partials
+    O, L = A.decode(q.cpu(), k.cpu(), v.cpu(), scale, splits)
+    for _ in range(2):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, h_q), float("nan"), device="cuda")
+        ra.attn_decode_splitkv(q, k, v, o, ws, lse, num_splits=splits, scale=scale)
+        close_o(o, O)
+        close_lse(lse, L)
+    rows = splits * B * h_q
+    off = ((rows * 8 + 15) // 16) * 16 + rows * D * 4
+    counters = ws[off:off + B * h_kv * 4].view(torch.int32)
+    assert (counters == 0).all()
+    assert ra.attn_last_device_status() == 0
+
+
 # ---------------------------------------------------------------------- failure detection
 def test_bounded_wait_times_out_cleanly_and_context_survives():
     assert ra.attn_last_device_status() == 0
