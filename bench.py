@@ -179,16 +179,25 @@ def make_workload(name: str, device, batch=None, seq=None):
         lse = torch.empty(cfg["B"], cfg["h_q"], cfg["S_q"], device=device, dtype=torch.float32)
         C = cfg["num_chunks"]
         causal = cfg["causal"]
+        window = cfg.get("window")
 
         def step(stream=None):
-            ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C, stream=stream)
+            if window is None:
+                ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C, stream=stream)
+            else:
+                ra.attn_prefill_window(q, k, v, o, lse, window=window, num_chunks=C, stream=stream)
         flops = 4.0 * cfg["D"] * cfg["B"] * cfg["h_q"] * causal_pairs(cfg["S_q"]) if causal else \
             4.0 * cfg["D"] * cfg["B"] * cfg["h_q"] * cfg["S_q"] * cfg["S_kv"]
+        if window is not None:  # query i sees min(i, window) + 1 keys
+            S = cfg["S_q"]
+            pairs = window * (window + 1) // 2 + (S - window) * (window + 1) if S > window else S * (S + 1) // 2
+            flops = 4.0 * cfg["D"] * cfg["B"] * cfg["h_q"] * pairs
         w.update(step=step, units=flops / 1e12, unit="TFLOP/s", bound="tensor", launches=1, tensors=(q, k, v, o, lse),
                  inputs=(q, k, v), outputs=(o, lse), kernel_units=flops / 1e12,
-                 config={"workload": name, "B": cfg["B"], "S": cfg["S_q"], "h_q": cfg["h_q"], "h_kv": cfg["h_kv"],
-                         "D": cfg["D"], "causal": causal, "num_chunks": C, "tile": "128x128",
-                         "l2": "inputs larger than L2 (no flush)"})
+                 config=dict({"workload": name, "B": cfg["B"], "S": cfg["S_q"], "h_q": cfg["h_q"],
+                              "h_kv": cfg["h_kv"], "D": cfg["D"], "causal": causal, "num_chunks": C,
+                              "tile": "128x128", "l2": "inputs larger than L2 (no flush)"},
+                             **({"window": window} if window is not None else {})))
         def e2e_step(host_in, host_out, stream):
             for d, h in zip((q, k, v), host_in):
                 d.copy_(h, non_blocking=True)
@@ -395,7 +404,7 @@ def run_ours(args):
     if not args.no_secondary and args.workload == HEADLINE and args.batch is None and args.seq is None:
         sec = []
         for name in ("jagged_causal_1152seq_h4_d128", "long_gqa_ring8_s32768_hq64_hkv8_d128",
-                     "decode_splitkv_b8_hq64_hkv8_d128_kv1m"):
+                     "decode_splitkv_b8_hq64_hkv8_d128_kv1m", "window4096_gqa_s32768_hq64_hkv8_d128"):
             w = make_workload(name, device)
             k2 = max(3, min(K, 20))
             ms2 = time_steps(w["step"], k2, W, device)

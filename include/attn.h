@@ -91,6 +91,22 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
                            int num_chunks, attn_stream_t stream);
 
 /*
+ * attn_prefill_window - causal prefill with a sliding window.
+ *   [BOUNDS] ("Scalar minimum": the dependent lower bound max(kv_begin,
+ *            tile_q.begin - window) deferred there to sliding-window support)
+ *
+ * As attn_prefill with causal = 1, except that key j is visible to query i only
+ * if i - window <= j <= i: each query sees its own key and the `window` keys
+ * before it.  Inside every chunk the walk starts at the first tile of the chunk's
+ * ATTN_BLOCK_N grid that holds a key the Q tile's first row can see; tiles at the
+ * window's lower edge are masked per row.  window >= S_kv is plain causal
+ * attention.  window < 0 is ATTN_ERR_INVALID_ARG; other arguments as attn_prefill.
+ */
+attn_status_t attn_prefill_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
+                                  int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale, int window,
+                                  int num_chunks, attn_stream_t stream);
+
+/*
  * attn_partial - the partial triplet of one KV range (one ring step's partial).
  *   [PREFILL] (step 0 partial / per-step partial on the rotated KV block)
  *
@@ -216,14 +232,15 @@ const char* attn_status_string(attn_status_t status);
  *   [BOUNDS] (dependent end, trip count); [PREFILL] (ring order, P6b)
  *
  * Q rows [q_lo, q_hi) at positions q_pos0 + i; keys [kv_lo, kv_hi) at positions
- * kv_pos0 + j, cut into num_chunks ring chunks.  Writes up to max_tiles entries
+ * kv_pos0 + j, cut into num_chunks ring chunks; window >= 0 (causal only) applies
+ * attn_prefill_window's sliding window, window = -1 none.  Writes up to max_tiles entries
  * (chunk, tile_start, mask_end) in visiting order, where mask_end is the first
  * key index that the tile's tail mask excludes, and stores the full count in
  * *n_tiles.  Returns ATTN_ERR_INVALID_ARG on bad sizes or null pointers.
  */
 attn_status_t attn_tile_walk(int q_lo, int q_hi, int kv_lo, int kv_hi, int block_n, int causal, int num_chunks,
-                             int q_pos0, int kv_pos0, int* chunk, int* tile_start, int* mask_end, int max_tiles,
-                             int* n_tiles);
+                             int q_pos0, int kv_pos0, int window, int* chunk, int* tile_start, int* mask_end,
+                             int max_tiles, int* n_tiles);
 
 #ifdef __cplusplus
 }

@@ -15,6 +15,11 @@ query's (top-left alignment: the same index space for Q and KV, as in the
 dependent inner-loop end min(kv_end, tile_q.end) of "[pallas] Support dependent
 Tile.end bounds in Pallas", opening example).  Query head h reads KV head
 floor(h / G), G = h_q / h_kv (contiguous head groups).
+Sliding window (optional, causal only): key j is visible to query i iff
+pos(i) - window <= pos(j) <= pos(i), i.e. the `window` keys before the query and
+the query's own.  This is the dependent lower bound max(kv_begin, tile_q.begin -
+window) that "[pallas] Support dependent Tile.end bounds in Pallas" ("Scalar
+minimum") defers to sliding-window support, taken at element level.
 
 Sources (page title, section):
   * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel:
@@ -54,11 +59,19 @@ def _kv_head(h: int, group: int) -> int:
     return h // group
 
 
-def _visible(q_pos: np.ndarray, k_pos: np.ndarray, causal: bool) -> np.ndarray:
-    """[len(q_pos), len(k_pos)] visibility: all pairs, or key position <= query position."""
+def _visible(q_pos: np.ndarray, k_pos: np.ndarray, causal: bool, window: int | None = None) -> np.ndarray:
+    """[len(q_pos), len(k_pos)] visibility: all pairs, or key position <= query position,
+    and with a window also key position >= query position - window."""
     if not causal:
+        if window is not None:
+            raise ValueError("a sliding window needs causal masking")
         return np.ones((q_pos.size, k_pos.size), dtype=bool)
-    return k_pos[None, :] <= q_pos[:, None]
+    vis = k_pos[None, :] <= q_pos[:, None]
+    if window is not None:
+        if window < 0:
+            raise ValueError("window must be >= 0")
+        vis &= k_pos[None, :] >= q_pos[:, None] - window
+    return vis
 
 
 def _scores(q_rows: np.ndarray, k_rows: np.ndarray, scale: float) -> np.ndarray:
@@ -84,7 +97,7 @@ def _row_triplet(s: np.ndarray, vis: np.ndarray, v_rows: np.ndarray):
 
 
 def attention(q, k, v, scale: float, causal: bool = False, q_pos0: int = 0,
-              kv_pos0: int = 0, rows=None, heads=None, batches=None):
+              kv_pos0: int = 0, rows=None, heads=None, batches=None, window: int | None = None):
     """Exact softmax attention, written out from its definition.
 
     O_i = sum_j softmax_j(s_i) v_j over the visible keys j, LSE_i = ln sum_j e^{s_ij}.
@@ -104,7 +117,7 @@ def attention(q, k, v, scale: float, causal: bool = False, q_pos0: int = 0,
     batches = range(B) if batches is None else batches
     out = np.full((B, S_q, h_q, v.shape[-1]), np.nan)
     lse = np.full((B, h_q, S_q), np.nan)
-    vis = _visible(q_pos0 + rows, kv_pos0 + np.arange(S_kv), causal)
+    vis = _visible(q_pos0 + rows, kv_pos0 + np.arange(S_kv), causal, window)
     for b in batches:
         for h in heads:
             g = _kv_head(h, group)
@@ -299,6 +312,13 @@ def causal_useful_flops(lengths_q_kv, head_dim: int, heads: int, causal: bool = 
             pairs += sum(min(i + 1, s_kv) for i in range(s_q)) if s_q != s_kv else s_q * (s_q + 1) // 2
         else:
             pairs += s_q * s_kv
+    return 4.0 * head_dim * heads * pairs
+
+
+def window_useful_flops(length: int, window: int, head_dim: int, heads: int) -> float:
+    """4 * D * H * (visible pairs) of one causal sequence under a sliding window:
+    query i sees min(i, window) + 1 keys."""
+    pairs = sum(min(i, window) + 1 for i in range(length))
     return 4.0 * head_dim * heads * pairs
 
 

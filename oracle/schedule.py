@@ -33,15 +33,22 @@ def cdiv(a: int, b: int) -> int:
 
 
 def pair_visible_in(q_lo: int, q_hi: int, k_lo: int, k_hi: int, causal: bool,
-                    q_pos0: int = 0, kv_pos0: int = 0) -> bool:
-    """True iff some query in [q_lo, q_hi) sees some key in [k_lo, k_hi)."""
+                    q_pos0: int = 0, kv_pos0: int = 0, window: int | None = None) -> bool:
+    """True iff some query in [q_lo, q_hi) sees some key in [k_lo, k_hi).
+
+    With a sliding window (causal only) key position p is visible to query
+    position i iff i - window <= p <= i.
+    """
     if q_hi <= q_lo or k_hi <= k_lo:
         return False
     if not causal:
         return True
     qpos = np.arange(q_lo, q_hi, dtype=np.int64) + q_pos0
     kpos = np.arange(k_lo, k_hi, dtype=np.int64) + kv_pos0
-    return bool((kpos[None, :] <= qpos[:, None]).any())
+    vis = kpos[None, :] <= qpos[:, None]
+    if window is not None:
+        vis &= kpos[None, :] >= qpos[:, None] - window
+    return bool(vis.any())
 
 
 def ring_chunks(kv_lo: int, kv_hi: int, num_chunks: int):
@@ -60,7 +67,7 @@ def ring_start_chunk(q_lo: int, kv_lo: int, kv_hi: int, num_chunks: int,
 
 
 def tile_walk(q_lo: int, q_hi: int, kv_lo: int, kv_hi: int, block_n: int, causal: bool,
-              num_chunks: int = 1, q_pos0: int = 0, kv_pos0: int = 0):
+              num_chunks: int = 1, q_pos0: int = 0, kv_pos0: int = 0, window: int | None = None):
     """Ordered KV tiles visited by the Q tile [q_lo, q_hi).
 
     Chunks are walked in ring order starting at the Q tile's own chunk; inside
@@ -78,7 +85,7 @@ def tile_walk(q_lo: int, q_hi: int, kv_lo: int, kv_hi: int, block_n: int, causal
         start = lo
         while start < hi:
             stop = min(start + block_n, hi)
-            if pair_visible_in(q_lo, q_hi, start, stop, causal, q_pos0, kv_pos0):
+            if pair_visible_in(q_lo, q_hi, start, stop, causal, q_pos0, kv_pos0, window):
                 walk.append((c, start, stop))
             start += block_n
     return walk

@@ -20,7 +20,7 @@ import os
 
 __all__ = [
     "AttnError", "load_library", "library_path",
-    "attn_prefill", "attn_partial", "attn_merge", "attn_jagged", "attn_decode_splitkv",
+    "attn_prefill", "attn_prefill_window", "attn_partial", "attn_merge", "attn_jagged", "attn_decode_splitkv",
     "attn_jagged_workspace_bytes", "attn_decode_workspace_bytes", "attn_decode_splitkv_noalloc",
     "attn_last_device_status", "attn_status_string", "attn_tile_walk", "attn_selftest_wait_timeout",
     "BLOCK_M", "BLOCK_N", "STATUS",
@@ -58,7 +58,8 @@ _SIGNATURES = {
     "attn_decode_splitkv_noalloc": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P],
     "attn_last_device_status": [_P],
     "attn_status_string": [_I],
-    "attn_tile_walk": [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P],
+    "attn_prefill_window": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P],
+    "attn_tile_walk": [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P],
     "attn_selftest_wait_timeout": [ctypes.c_uint64, _P],
 }
 
@@ -131,6 +132,18 @@ def attn_prefill(q, k, v, o, lse=None, *, scale=None, causal=False, num_chunks=1
                                      _dtype_code(q), _scale(scale, D), int(bool(causal)), int(num_chunks),
                                      _stream(stream, q))
     _check(st, "attn_prefill")
+
+
+def attn_prefill_window(q, k, v, o, lse=None, *, window, scale=None, num_chunks=1, stream=None):
+    """Causal prefill where query i sees keys i - window .. i (see attn.h)."""
+    _cuda_contig(q, k, v, o, lse)
+    B, S_q, h_q, D = q.shape
+    S_kv, h_kv = k.shape[1], k.shape[2]
+    _need(k.shape == v.shape and o.shape == q.shape and k.shape[0] == B and k.shape[3] == D, "shape mismatch")
+    st = load_library().attn_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, S_q, S_kv, h_q, h_kv,
+                                            D, _dtype_code(q), _scale(scale, D), int(window), int(num_chunks),
+                                            _stream(stream, q))
+    _check(st, "attn_prefill_window")
 
 
 def attn_partial(q, k, v, m, l, o_unnorm, *, scale=None, causal=False, q_pos0=0, kv_begin=0, kv_end=None,
@@ -219,16 +232,18 @@ def attn_status_string(status: int) -> str:
     return load_library().attn_status_string(int(status)).decode()
 
 
-def attn_tile_walk(q_lo, q_hi, kv_lo, kv_hi, *, block_n=BLOCK_N, causal=True, num_chunks=1, q_pos0=0, kv_pos0=0):
+def attn_tile_walk(q_lo, q_hi, kv_lo, kv_hi, *, block_n=BLOCK_N, causal=True, num_chunks=1, q_pos0=0, kv_pos0=0,
+                   window=None):
     """KV tiles (chunk, tile_start, mask_end) one Q tile visits, from the library's scheduler (host code)."""
     lib = load_library()
     n = ctypes.c_int(0)
-    st = lib.attn_tile_walk(q_lo, q_hi, kv_lo, kv_hi, block_n, int(bool(causal)), num_chunks, q_pos0, kv_pos0,
+    w = -1 if window is None else int(window)
+    st = lib.attn_tile_walk(q_lo, q_hi, kv_lo, kv_hi, block_n, int(bool(causal)), num_chunks, q_pos0, kv_pos0, w,
                             None, None, None, 0, ctypes.byref(n))
     _check(st, "attn_tile_walk")
     cap = n.value
     arr = [(ctypes.c_int * max(cap, 1))() for _ in range(3)]
-    st = lib.attn_tile_walk(q_lo, q_hi, kv_lo, kv_hi, block_n, int(bool(causal)), num_chunks, q_pos0, kv_pos0,
+    st = lib.attn_tile_walk(q_lo, q_hi, kv_lo, kv_hi, block_n, int(bool(causal)), num_chunks, q_pos0, kv_pos0, w,
                             arr[0], arr[1], arr[2], cap, ctypes.byref(n))
     _check(st, "attn_tile_walk")
     return [(arr[0][i], arr[1][i], arr[2][i]) for i in range(cap)]

@@ -116,16 +116,10 @@ size_t jagged_max_items(int num_seqs, int total_tokens, int block_m = ATTN_BLOCK
   return ((size_t)total_tokens + (size_t)num_seqs * (block_m - 1)) / block_m;
 }
 
-}  // namespace
-}  // namespace attn
-
-using namespace attn;
-
-extern "C" {
-
-attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
+// attn_prefill and attn_prefill_window: window < 0 is none.
+attn_status_t prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
                            int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale, int causal,
-                           int num_chunks, attn_stream_t stream) {
+                           int window, int num_chunks, attn_stream_t stream) {
   attn_status_t st = check_dense(q, k, v, B, S_q, S_kv, h_q, h_kv, D, dtype, scale, causal);
   if (st != ATTN_OK) return st;
   if (!o || !aligned(o, 16) || (lse && !aligned(lse, 4)) || num_chunks < 1) return ATTN_ERR_INVALID_ARG;
@@ -148,13 +142,35 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   p.kv_hi = S_kv;
   p.scale_log2 = scale * kLog2e;
   p.pair_heads = (p.group % 2) == 0;
+  p.window = window;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
   dim3 grid;
   if (!dense_grid(p, D, &grid)) return ATTN_ERR_UNSUPPORTED;
-  return launch_prefill(p, mq, mk, mv, kModeDense, bf16, D, grid, reinterpret_cast<cudaStream_t>(stream));
+  return launch_prefill(p, mq, mk, mv, window >= 0 ? kModeWindow : kModeDense, bf16, D, grid,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
+                           int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale, int causal,
+                           int num_chunks, attn_stream_t stream) {
+  return prefill_impl(q, k, v, o, lse, B, S_q, S_kv, h_q, h_kv, D, dtype, scale, causal, -1, num_chunks, stream);
+}
+
+attn_status_t attn_prefill_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_q,
+                                  int S_kv, int h_q, int h_kv, int D, attn_dtype_t dtype, float scale, int window,
+                                  int num_chunks, attn_stream_t stream) {
+  if (window < 0) return ATTN_ERR_INVALID_ARG;
+  return prefill_impl(q, k, v, o, lse, B, S_q, S_kv, h_q, h_kv, D, dtype, scale, 1, window, num_chunks, stream);
 }
 
 attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o_unnorm,
@@ -318,13 +334,14 @@ const char* attn_status_string(attn_status_t status) {
 }
 
 attn_status_t attn_tile_walk(int q_lo, int q_hi, int kv_lo, int kv_hi, int block_n, int causal, int num_chunks,
-                             int q_pos0, int kv_pos0, int* chunk, int* tile_start, int* mask_end, int max_tiles,
-                             int* n_tiles) {
+                             int q_pos0, int kv_pos0, int window, int* chunk, int* tile_start, int* mask_end,
+                             int max_tiles, int* n_tiles) {
   if (!n_tiles || block_n < 1 || num_chunks < 1 || q_hi < q_lo || kv_hi < kv_lo || max_tiles < 0 ||
-      (max_tiles > 0 && (!chunk || !tile_start || !mask_end)) || (causal != 0 && causal != 1))
+      (max_tiles > 0 && (!chunk || !tile_start || !mask_end)) || (causal != 0 && causal != 1) || window < -1 ||
+      (window >= 0 && !causal))
     return ATTN_ERR_INVALID_ARG;
   TileWalk w;
-  w.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, causal, num_chunks, block_n);
+  w.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, causal, num_chunks, block_n, window);
   const int total = w.count();
   int i = 0, c, st, me;
   while (i < max_tiles && w.next(c, st, me)) {

@@ -21,7 +21,9 @@ enum : unsigned int {
 // microseconds, so only a broken pipeline ever reaches it.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
 
-enum PrefillMode : int { kModeDense = 0, kModePartial = 1, kModeJagged = 2 };
+// kModeWindow is dense prefill with a causal sliding window (a separate
+// instantiation, so the other modes carry none of its checks)
+enum PrefillMode : int { kModeDense = 0, kModePartial = 1, kModeJagged = 2, kModeWindow = 3 };
 
 struct PrefillParams {
   // outputs
@@ -39,6 +41,7 @@ struct PrefillParams {
   // pairs (pair_heads) or heads
   int n_items, n_qt, n_y;
   int q_pos0, kv_pos0, kv_lo, kv_hi;  // dense / partial key range and positions
+  int window;                         // kModeWindow: query q sees keys q - window .. q
   float scale_log2;                   // softmax scale * log2(e)
   // jagged worklist: count followed by items {seq_begin, seq_len, tile_start, tile_extent}
   const int* work_count;

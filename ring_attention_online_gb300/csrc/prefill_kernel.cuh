@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(352, 1)
   }
   const int hk = h / p.group;
   TileWalk walk;
-  walk.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, p.num_chunks, C::BN);
+  walk.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, p.num_chunks, C::BN, kMode == kModeWindow ? p.window : -1);
   const int n = walk.count();
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -307,22 +307,27 @@ __global__ void __launch_bounds__(352, 1)
       tmem_ld_wait(r0);
       tmem_ld_wait(r1);
 
-      // mask the diagonal / tail tile: key kstart + i is visible iff i < lim
+      // mask the diagonal / tail tile (key kstart + i is visible iff i < lim)
+      // and, under a sliding window, the tiles at its lower edge (iff i >= flo)
+      constexpr bool win = kMode == kModeWindow;
       const bool need_mask =
           (kstart + C::BN > mend) ||
-          (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo));
+          (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo)) ||
+          (win && (long long)kv_pos0 + kstart < (long long)q_pos0 + q_hi - 1 - p.window);
       if (need_mask) {
         long long lim = (long long)mend - kstart;
+        long long flo = 0;
         if (p.causal) {
           const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
           lim = lc < lim ? lc : lim;
+          if (win) flo = lc - 1 - p.window;
         }
-        const long long lh = lim - half * 64;  // limit within this half
+        const long long lh = lim - half * 64, fh = flo - half * 64;  // limits within this half
         const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (i >= lh) r0[i] = ninf;
-          if (i + 32 >= lh) r1[i] = ninf;
+          if (i >= lh || i < fh) r0[i] = ninf;
+          if (i + 32 >= lh || i + 32 < fh) r1[i] = ninf;
         }
       }
       float mx8[8];
@@ -506,12 +511,14 @@ attn_status_t launch_prefill_dispatch(const PrefillParams& p, const CUtensorMap&
       case kModeDense: return launch_prefill_variant<D, true, kModeDense>(p, mq, mk, mv, grid, s);
       case kModePartial: return launch_prefill_variant<D, true, kModePartial>(p, mq, mk, mv, grid, s);
       case kModeJagged: return launch_prefill_variant<D, true, kModeJagged>(p, mq, mk, mv, grid, s);
+      case kModeWindow: return launch_prefill_variant<D, true, kModeWindow>(p, mq, mk, mv, grid, s);
     }
   } else {
     switch (mode) {
       case kModeDense: return launch_prefill_variant<D, false, kModeDense>(p, mq, mk, mv, grid, s);
       case kModePartial: return launch_prefill_variant<D, false, kModePartial>(p, mq, mk, mv, grid, s);
       case kModeJagged: return launch_prefill_variant<D, false, kModeJagged>(p, mq, mk, mv, grid, s);
+      case kModeWindow: return launch_prefill_variant<D, false, kModeWindow>(p, mq, mk, mv, grid, s);
     }
   }
   return ATTN_ERR_INVALID_ARG;

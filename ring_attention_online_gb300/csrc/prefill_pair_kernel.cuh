@@ -187,13 +187,17 @@ __global__ void __launch_bounds__(352, 1)
   auto item_walk = [&](const PairItem& it, TileWalk& walk) -> int {
     const int u_lo = it.st0.q_lo;
     const int u_hi = it.st1.empty() ? it.st0.q_hi : max(it.st0.q_hi, it.st1.q_hi);
-    walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, p.num_chunks, C::BN);
+    walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, p.num_chunks, C::BN,
+              kMode == kModeWindow ? p.window : -1);
     return walk.count();
   };
   auto active = [&](const PairItem& it, int x, int ks) -> bool {
     const SubTile t = x ? it.st1 : it.st0;
     if (t.empty()) return false;
-    return !p.causal || (long long)it.kv_pos0 + ks <= (long long)it.q_pos0 + t.q_hi - 1;
+    if (!p.causal) return true;
+    if ((long long)it.kv_pos0 + ks > (long long)it.q_pos0 + t.q_hi - 1) return false;
+    // under a sliding window, the tile's last key must reach the first row's window
+    return kMode != kModeWindow || (long long)it.kv_pos0 + ks + C::BN - 1 >= (long long)it.q_pos0 + t.q_lo - p.window;
   };
 
   if (warp == 0) {
@@ -398,15 +402,19 @@ __global__ void __launch_bounds__(352, 1)
         // S_x(j) was issued after this sub-tile's previous P.V by the same
         // thread, so its completion also means that P.V has finished: O may
         // be rescaled without waiting on bar_o.
+        constexpr bool win = kMode == kModeWindow;
         const bool need_mask =
             (kstart + C::BN > mend) ||
-            (p.causal && ((long long)it.kv_pos0 + kstart + C::BN - 1 > (long long)it.q_pos0 + me_t.q_lo));
-        long long lim = C::BN;  // key kstart + i is visible iff i < lim
+            (p.causal && ((long long)it.kv_pos0 + kstart + C::BN - 1 > (long long)it.q_pos0 + me_t.q_lo)) ||
+            (win && (long long)it.kv_pos0 + kstart < (long long)it.q_pos0 + me_t.q_hi - 1 - p.window);
+        long long lim = C::BN;  // key kstart + i is visible iff flo <= i < lim
+        long long flo = 0;
         if (need_mask) {
           lim = (long long)mend - kstart;
           if (p.causal) {
             const long long lc = (long long)it.q_pos0 + q_row - it.kv_pos0 - kstart + 1;
             lim = lc < lim ? lc : lim;
+            if (win) flo = lc - 1 - p.window;
           }
         }
         // the first 64 columns are reduced while the second pair of loads is in flight
@@ -420,8 +428,8 @@ __global__ void __launch_bounds__(352, 1)
         if (need_mask) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (i >= lim) r0[i] = ninf;
-            if (i + 32 >= lim) r1[i] = ninf;
+            if (i >= lim || i < flo) r0[i] = ninf;
+            if (i + 32 >= lim || i + 32 < flo) r1[i] = ninf;
           }
         }
         float mx8[8];
@@ -436,8 +444,8 @@ __global__ void __launch_bounds__(352, 1)
         if (need_mask) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (i + 64 >= lim) r2[i] = ninf;
-            if (i + 96 >= lim) r3[i] = ninf;
+            if (i + 64 >= lim || i + 64 < flo) r2[i] = ninf;
+            if (i + 96 >= lim || i + 96 < flo) r3[i] = ninf;
           }
         }
 #pragma unroll
@@ -600,12 +608,14 @@ attn_status_t launch_pair_dispatch(const PrefillParams& p, const CUtensorMap& mq
       case kModeDense: return launch_pair_variant<D, true, kModeDense>(p, mq, mk, mv, grid, s);
       case kModePartial: return launch_pair_variant<D, true, kModePartial>(p, mq, mk, mv, grid, s);
       case kModeJagged: return launch_pair_variant<D, true, kModeJagged>(p, mq, mk, mv, grid, s);
+      case kModeWindow: return launch_pair_variant<D, true, kModeWindow>(p, mq, mk, mv, grid, s);
     }
   } else {
     switch (mode) {
       case kModeDense: return launch_pair_variant<D, false, kModeDense>(p, mq, mk, mv, grid, s);
       case kModePartial: return launch_pair_variant<D, false, kModePartial>(p, mq, mk, mv, grid, s);
       case kModeJagged: return launch_pair_variant<D, false, kModeJagged>(p, mq, mk, mv, grid, s);
+      case kModeWindow: return launch_pair_variant<D, false, kModeWindow>(p, mq, mk, mv, grid, s);
     }
   }
   return ATTN_ERR_INVALID_ARG;

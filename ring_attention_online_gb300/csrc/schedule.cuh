@@ -6,6 +6,12 @@
 // trip_count = cdiv(active_end - begin, block_k) tiles, the last one masked by
 // indices_k < active_end.  Fully masked tiles are never visited (pruned).
 //
+// Sliding window (causal, window >= 0): a key is visible to a query iff
+// q - window <= k <= q, the dependent lower bound max(kv_begin, tile_q.begin -
+// window) that the same page ("Scalar minimum") defers to sliding-window
+// support.  A chunk's tiles still start on its block_n grid; the walk starts at
+// the tile holding the first key the Q tile's first row can see.
+//
 // "kernbench2 _gqa_prefill_long.py" (module docstring, P6b; ring loop): a
 // unit that starts on its own KV block and receives from its east neighbour
 // sees blocks (c + t) mod C.  Here the C chunks of one KV range are walked in
@@ -24,11 +30,12 @@ struct TileWalk {
   int kv_lo, kv_hi, block_n, num_chunks;
   int chunk_len, c0;
   int key_limit;  // keys with index >= key_limit are invisible to every row of the tile
+  int key_floor;  // keys with index < key_floor are invisible to every row (sliding window)
   // cursor
   int t, chunk, cur, end;
 
   __host__ __device__ void init(int q_lo, int q_hi, int kv_lo_, int kv_hi_, int q_pos0, int kv_pos0, int causal,
-                                int num_chunks_, int block_n_) {
+                                int num_chunks_, int block_n_, int window = -1) {
     kv_lo = kv_lo_;
     kv_hi = kv_hi_;
     block_n = block_n_;
@@ -46,6 +53,13 @@ struct TileWalk {
     } else {
       key_limit = q_hi <= q_lo ? INT_MIN : INT_MAX;
     }
+    key_floor = INT_MIN;
+    if (causal && window >= 0) {
+      // the tile's first query sits at q_pos0 + q_lo and sees keys from position
+      // q_pos0 + q_lo - window on
+      const long long fl = (long long)q_pos0 + q_lo - window - kv_pos0;
+      key_floor = (int)(fl > INT_MAX ? INT_MAX : (fl < INT_MIN ? INT_MIN : fl));
+    }
     t = 0;
     open_chunk();
   }
@@ -59,8 +73,14 @@ struct TileWalk {
       const long long hi_ll = lo_ll + chunk_len;
       const int hi = (int)(hi_ll < kv_hi ? hi_ll : kv_hi);
       end = hi < key_limit ? hi : key_limit;  // min(chunk_end, tile_q.end)
-      if (end > lo) {
-        cur = lo;
+      int start = lo;
+      if (key_floor > lo) {  // first tile of the chunk's grid that holds a key >= key_floor
+        const long long skip = ((long long)key_floor - lo) / block_n;
+        const long long st = lo + skip * block_n;
+        start = (int)(st < end ? st : end);
+      }
+      if (end > start && key_floor < end) {
+        cur = start;
         return;
       }
       ++t;

@@ -39,6 +39,11 @@ WORKLOADS = {
                                                  causal=True, num_chunks=8),
     "decode_splitkv_b8_hq64_hkv8_d128_kv1m": dict(kind="decode", B=8, h_q=64, h_kv=8, D=128,
                                                   S_kv=1 << 20, dtype="bf16", num_splits=64),
+    # the long GQA prefill with a causal sliding window of 4096 keys (no page states a
+    # window workload; this is the long-context shape with a typical window size)
+    "window4096_gqa_s32768_hq64_hkv8_d128": dict(kind="prefill", B=1, S_q=32768, S_kv=32768,
+                                                 h_q=64, h_kv=8, D=128, dtype="bf16",
+                                                 causal=True, num_chunks=1, window=4096),
 }
 
 

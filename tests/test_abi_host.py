@@ -126,6 +126,32 @@ def test_tile_walk_matches_oracle_bit_exact(lib, seed):
                 assert not S.pair_visible_in(lo, hi, mend, stop, causal, q_pos0, 0)
 
 
+@pytest.mark.parametrize("seed", range(40))
+def test_window_tile_walk_matches_oracle_bit_exact(lib, seed):
+    """Sliding window: the library's walk starts at the grid tile holding the first
+    visible key and keeps exactly the tiles that hold a visible (query, key) pair."""
+    rng = np.random.default_rng(1000 + seed)
+    L = int(rng.integers(1, 1200))
+    C = int(rng.integers(1, 6))
+    window = int(rng.choice([0, 1, 63, 127, 128, 129, 255, 300, 1000, 5000]))
+    q_pos0 = int(rng.integers(-200, 200)) if rng.random() < 0.3 else 0
+    for lo, hi in S.dense_work_items(L, 128):
+        got = ra.attn_tile_walk(lo, hi, 0, L, block_n=128, causal=True, num_chunks=C, q_pos0=q_pos0, window=window)
+        ref = S.tile_walk(lo, hi, 0, L, 128, True, C, q_pos0, 0, window)
+        assert [(c, st) for c, st, _ in got] == [(c, st) for c, st, _ in ref]
+
+
+def test_window_validation(lib):
+    n = ctypes.c_int(0)
+    assert lib.attn_tile_walk(0, 128, 0, 512, 128, 0, 1, 0, 0, 5, None, None, None, 0, ctypes.byref(n)) == 1  # window needs causal
+    assert lib.attn_tile_walk(0, 128, 0, 512, 128, 1, 1, 0, 0, -2, None, None, None, 0, ctypes.byref(n)) == 1
+    args = [FAKE, FAKE, FAKE, FAKE, None, 1, 128, 128, 2, 1, 128, 1, 0.1, -1, 1, None]
+    assert lib.attn_prefill_window(*args) == 1  # negative window
+    args[13] = 0
+    args[10] = 96
+    assert lib.attn_prefill_window(*args) == 2  # D outside {64,128,256}
+
+
 def test_tile_walk_full_size_counts(lib):
     # dense causal S=4096: 528 tiles per (batch, head); ring S=32768, C=8: 32896 tiles
     tot = sum(len(ra.attn_tile_walk(lo, hi, 0, 4096, causal=True)) for lo, hi in S.dense_work_items(4096, 128))

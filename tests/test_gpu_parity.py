@@ -84,6 +84,37 @@ def test_prefill_ring_gqa(C, causal):
     close_lse(lse, L)
 
 
+# ---------------------------------------------------------------------- sliding window
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 129, 300, 5000])
+@pytest.mark.parametrize("h_q,h_kv", [(4, 2), (2, 2)])
+def test_prefill_window_parity(D, window, h_q, h_kv):
+    """Both kernels (paired for 64/128 with head pairs and Q-tile pairs, single-tile for
+    256): the walk floor, the per-row lower mask and sub-tiles sitting out tiles below
+    their window; window 5000 > S is plain causal."""
+    B, S_ = 1, 650
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=window + D)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    scale = 1 / math.sqrt(D)
+    ra.attn_prefill_window(q, k, v, o, lse, window=window, scale=scale)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), scale, True, window=window)
+    close_o(o, O, f"window={window} D={D}")
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("C", [1, 3, 8])
+def test_prefill_window_ring_gqa(C):
+    B, S_, h_q, h_kv, D, window = 1, 2000, 8, 2, 128, 700
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=40 + C)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill_window(q, k, v, o, lse, window=window, num_chunks=C)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), True, window=window)
+    close_o(o, O, f"window ring C={C}")
+    close_lse(lse, L)
+
+
 @pytest.mark.parametrize("S_q,S_kv", [(200, 700), (700, 200), (1, 513), (129, 1)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_prefill_unequal_lengths(S_q, S_kv, causal):

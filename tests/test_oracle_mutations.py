@@ -13,7 +13,7 @@ import pytest
 
 from oracle import attention as A
 from oracle import schedule as S
-from tests.test_oracle_pins import brute_attention
+from tests.test_oracle_pins import brute_attention, brute_window
 
 RNG = np.random.default_rng(7)
 
@@ -42,6 +42,17 @@ def _pins_pass():
         w = S.tile_walk(256, 384, 0, 512, 128, True, 4)
         if w != [(2, 256, 384), (0, 0, 128), (1, 128, 256)]:
             return False
+        for window in (0, 3):
+            q = RNG.standard_normal((1, 10, 2, 4))
+            k = RNG.standard_normal((1, 10, 1, 4))
+            v = RNG.standard_normal((1, 10, 1, 3))
+            O, L = A.attention(q, k, v, 0.6, True, window=window)
+            Ob, Lb = brute_window(q, k, v, 0.6, window)
+            if not (np.allclose(O, Ob, atol=1e-10) and np.allclose(L, Lb, atol=1e-10)):
+                return False
+        # a sliding window of 100 keys: a Q tile at rows [512, 640) sees keys from 412 on
+        if S.tile_walk(512, 640, 0, 1024, 128, True, 1, window=100) != [(0, 384, 512), (0, 512, 640)]:
+            return False
         return True
     except Exception:
         return False
@@ -60,8 +71,12 @@ def _scores_transposed(q_rows, k_rows, scale):
 MUTANTS = {
     # interleaved head groups (h mod h_kv) instead of contiguous ones; the pins use h_kv == G == 2
     "gqa_interleaved_groups": ("_kv_head", lambda h, g: h % g),
-    "causal_strict": ("_visible", lambda qp, kp, c: (kp[None, :] < qp[:, None]) if c else np.ones((qp.size, kp.size), bool)),
-    "causal_reversed": ("_visible", lambda qp, kp, c: (kp[None, :] >= qp[:, None]) if c else np.ones((qp.size, kp.size), bool)),
+    "causal_strict": ("_visible", lambda qp, kp, c, w=None: (kp[None, :] < qp[:, None]) if c else np.ones((qp.size, kp.size), bool)),
+    "causal_reversed": ("_visible", lambda qp, kp, c, w=None: (kp[None, :] >= qp[:, None]) if c else np.ones((qp.size, kp.size), bool)),
+    # sliding window one key short (strict lower bound) and window ignored
+    "window_strict": ("_visible", lambda qp, kp, c, w=None: (kp[None, :] <= qp[:, None]) & (
+        (kp[None, :] > qp[:, None] - w) if w is not None else True) if c else np.ones((qp.size, kp.size), bool)),
+    "window_ignored": ("_visible", lambda qp, kp, c, w=None: (kp[None, :] <= qp[:, None]) if c else np.ones((qp.size, kp.size), bool)),
     "scale_dropped": ("_scores", lambda q, k, s: q @ k.T),
     "scale_inverted": ("_scores", lambda q, k, s: (q @ k.T) / s),
     "k_reshaped_not_transposed": ("_scores", _scores_transposed),
@@ -106,6 +121,16 @@ def test_planted_schedule_mistakes_are_caught(monkeypatch):
     monkeypatch.undo()
     # visibility test that ignores causality
     monkeypatch.setattr(S, "pair_visible_in", lambda q_lo, q_hi, k_lo, k_hi, causal, *a: q_hi > q_lo and k_hi > k_lo)
+    assert not _pins_pass()
+    monkeypatch.undo()
+    # window lower bound taken from the Q tile's last row instead of its first
+    real = S.pair_visible_in
+
+    def late_floor(q_lo, q_hi, k_lo, k_hi, causal, q_pos0=0, kv_pos0=0, window=None):
+        if window is None:
+            return real(q_lo, q_hi, k_lo, k_hi, causal, q_pos0, kv_pos0)
+        return real(q_hi - 1, q_hi, k_lo, k_hi, causal, q_pos0, kv_pos0, window)
+    monkeypatch.setattr(S, "pair_visible_in", late_floor)
     assert not _pins_pass()
 
 

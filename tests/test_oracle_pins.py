@@ -266,3 +266,66 @@ def test_causal_useful_flops_closed_forms():
     assert A.causal_useful_flops([(3, 5)], 2, 1, causal=False) == 4 * 2 * 15
     # a shorter query block against more keys (top-left): sum min(i+1, S_kv)
     assert A.causal_useful_flops([(3, 2)], 1, 1) == 4 * (1 + 2 + 2)
+
+
+# ---------------------------------------------------------------------- sliding window
+def brute_window(q, k, v, scale, window):
+    """Triple loop over (query, key, d): key j counts for query i iff i - window <= j <= i."""
+    B, S, h_q, D = q.shape
+    G = h_q // k.shape[2]
+    O = np.zeros(q.shape[:3] + (v.shape[3],))
+    L = np.zeros((B, h_q, S))
+    for b in range(B):
+        for h in range(h_q):
+            g = h // G
+            for i in range(S):
+                scores = [(j, scale * sum(float(q[b, i, h, d]) * float(k[b, j, g, d]) for d in range(D)))
+                          for j in range(S) if i - window <= j <= i]
+                mx = max(sc for _, sc in scores)
+                den = sum(math.exp(sc - mx) for _, sc in scores)
+                for e in range(v.shape[3]):
+                    O[b, i, h, e] = sum(math.exp(sc - mx) * float(v[b, j, g, e]) for j, sc in scores) / den
+                L[b, h, i] = mx + math.log(den)
+    return O, L
+
+
+@pytest.mark.parametrize("window", [0, 1, 3, 11, 40])
+def test_window_oracle_matches_brute_force(window):
+    rng = np.random.default_rng(window + 5)
+    q, k, v = rng.standard_normal((1, 12, 2, 4)), rng.standard_normal((1, 12, 1, 4)), rng.standard_normal((1, 12, 1, 5))
+    O, L = A.attention(q, k, v, 0.7, causal=True, window=window)
+    Ob, Lb = brute_window(q, k, v, 0.7, window)
+    assert np.abs(O - Ob).max() < 1e-12 and np.abs(L - Lb).max() < 1e-12
+
+
+@pytest.mark.parametrize("window", [0, 2, 7, 100])
+def test_window_zero_queries_closed_form(window):
+    """Q = 0: every visible key scores 0, so O_i is the mean of v over [i - window, i]
+    and LSE_i = ln(min(i, window) + 1)."""
+    rng = np.random.default_rng(9)
+    S = 20
+    q = np.zeros((2, S, 2, 8))
+    k, v = rng.standard_normal((2, S, 1, 8)), rng.standard_normal((2, S, 1, 3))
+    O, L = A.attention(q, k, v, 0.3, causal=True, window=window)
+    for i in range(S):
+        lo = max(0, i - window)
+        assert np.abs(O[:, i, :, :] - v[:, lo:i + 1, 0, :].mean(axis=1)[:, None, :]).max() < 1e-12
+        assert np.abs(L[:, :, i] - math.log(min(i, window) + 1)).max() < 1e-12
+
+
+def test_window_zero_is_the_diagonal_and_large_window_is_causal():
+    rng = np.random.default_rng(3)
+    q, k, v = rng.standard_normal((1, 9, 1, 6)), rng.standard_normal((1, 9, 1, 6)), rng.standard_normal((1, 9, 1, 6))
+    O0, L0 = A.attention(q, k, v, 0.5, causal=True, window=0)
+    assert np.abs(O0 - v).max() < 1e-12  # each query sees only its own key
+    assert np.abs(L0[0, 0] - 0.5 * np.einsum("sd,sd->s", q[0, :, 0], k[0, :, 0])).max() < 1e-12
+    Ow, Lw = A.attention(q, k, v, 0.5, causal=True, window=8)
+    Oc, Lc = A.attention(q, k, v, 0.5, causal=True)
+    assert np.array_equal(Ow, Oc) and np.array_equal(Lw, Lc)
+
+
+def test_window_useful_flops_closed_form():
+    # w(w+1)/2 + (L - w)(w + 1) pairs when L > w
+    L, w = 4096, 1000
+    assert A.window_useful_flops(L, w, 128, 2) == 4.0 * 128 * 2 * (w * (w + 1) // 2 + (L - w) * (w + 1))
+    assert A.window_useful_flops(50, 200, 64, 1) == A.causal_useful_flops([(50, 50)], 64, 1)
