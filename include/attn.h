@@ -144,9 +144,14 @@ attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, 
  *
  * Sequence b spans tokens [seq_offsets[b], seq_offsets[b+1]) and attends only to
  * itself.  Q tiles start at the sequence start.  A device kernel first builds the
- * flattened worklist (one item per (sequence, Q tile)) from the device-resident
- * seq_offsets into `workspace`; the attention kernel then runs one CTA per
- * (item, head).  No host synchronisation is needed.
+ * flattened worklist from the device-resident seq_offsets into `workspace`: one
+ * item per (sequence, Q tile) and one unit per sequence (its items, which are
+ * contiguous).  The attention kernel then runs, for D = 64/128, one persistent
+ * CTA per SM over (unit, head) pairs, a sequence's Q tiles back to back so its
+ * K/V is re-read from L2 ("Grouping": successive Q items reuse the resident K/V
+ * range); for D = 256 one CTA per (item, head).  No host synchronisation.
+ * Workspace: int item count, int unit count, 8 bytes pad, the int4 items, then
+ * the int2 units {first item, item count}.
  *   q/k/v/o [total_tokens,H,D]; lse [H,total_tokens] fp32 or NULL;
  *   seq_offsets int32 [num_seqs+1], device memory, non-decreasing, from 0 to at
  *   most total_tokens, every length <= max_seqlen (violations are reported as

@@ -225,7 +225,8 @@ attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, 
 size_t attn_jagged_workspace_bytes(int num_seqs, int total_tokens, int max_seqlen) {
   (void)max_seqlen;
   if (num_seqs < 0 || total_tokens < 0) return 0;
-  return 16 + 16 * jagged_max_items(num_seqs, total_tokens);
+  // counts, items (sized for 128-row Q tiles, the larger count), one unit per sequence
+  return 16 + 16 * jagged_max_items(num_seqs, total_tokens) + (((size_t)num_seqs * 8 + 15) & ~size_t(15));
 }
 
 attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -243,7 +244,7 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
   const int block = jagged_block(D);
   const size_t max_items = jagged_max_items(num_seqs, total_tokens, block);
   if (max_items > 0x7fffffffULL || H > 65535) return ATTN_ERR_UNSUPPORTED;
-  if (paired(D) && (unsigned long long)max_items * H > 0x7fffffffULL) return ATTN_ERR_UNSUPPORTED;
+  if (paired(D) && (unsigned long long)num_seqs * H > 0x7fffffffULL) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* wl = static_cast<int*>(workspace);
   st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, block, wl, (int)max_items, s);
@@ -263,12 +264,14 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
   p.scale_log2 = scale * kLog2e;
   p.work_count = wl;
   p.work_items = reinterpret_cast<const int4*>(wl + 4);
+  p.work_units = reinterpret_cast<const int2*>(wl + 4 + 4 * max_items);
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, bf16, D, H, total_tokens, 1, ATTN_BLOCK_M) ||
       !make_map(&mk, k, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N) ||
       !make_map(&mv, v, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  const dim3 grid = paired(D) ? persistent_grid((long long)max_items * H) : dim3((unsigned)max_items, H, 1);
+  // paired kernel: persistent over (sequence, head) units; otherwise one CTA per (item, head)
+  const dim3 grid = paired(D) ? persistent_grid((long long)num_seqs * H) : dim3((unsigned)max_items, H, 1);
   return launch_prefill(p, mq, mk, mv, kModeJagged, bf16, D, grid, s);
 }
 

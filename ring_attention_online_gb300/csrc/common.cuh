@@ -43,9 +43,11 @@ struct PrefillParams {
   int q_pos0, kv_pos0, kv_lo, kv_hi;  // dense / partial key range and positions
   int window;                         // kModeWindow: query q sees keys q - window .. q
   float scale_log2;                   // softmax scale * log2(e)
-  // jagged worklist: count followed by items {seq_begin, seq_len, tile_start, tile_extent}
+  // jagged worklist: item count, unit count; items {seq_begin, seq_len, tile_start,
+  // tile_extent}; units {first item, item count}, one per sequence
   const int* work_count;
   const int4* work_items;
+  const int2* work_units;
   unsigned int* status;
 };
 

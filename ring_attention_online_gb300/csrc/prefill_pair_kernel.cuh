@@ -73,24 +73,44 @@ struct PairItem {
   SubTile st0, st1;
 };
 
-// Number of work items of a launch (jagged: read from the device worklist).
+// Number of work units of a launch: jagged, (sequence, head) pairs from the
+// device worklist's unit table; otherwise single items.
 template <int kMode>
 __device__ __forceinline__ int pair_item_count(const PrefillParams& p) {
-  if constexpr (kMode == kModeJagged) return *p.work_count * p.h_q;
+  if constexpr (kMode == kModeJagged) return p.work_count[1] * p.h_q;
   return p.n_items;
 }
 
-// Item k of the launch.  Dense / partial items: the Q tiles of one head (pair)
-// and batch are consecutive, longest causal walk first, so the CTAs that run
-// at one time share the K/V of one head in L2.  Jagged items follow the
-// worklist (longest sequences first), all heads of one Q tile in a row.
+// Work unit k: items [i0, i0 + n) of head h.  A jagged unit is every Q tile of
+// one (sequence, head), taken back to back by one CTA so that the sequence's
+// K/V, read by its first (longest) tile, is re-read from L2 by the others
+// ("Grouping" in "[pallas] Support dependent Tile.end bounds in Pallas":
+// successive Q work items reuse the resident K/V range).  The worklist's item
+// count bounds the unit's items.
+struct PairUnit {
+  int i0, n, h;
+};
 template <int kMode>
-__device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int k) {
+__device__ __forceinline__ PairUnit pair_unit(const PrefillParams& p, int k) {
+  if constexpr (kMode == kModeJagged) {
+    const int2 u = p.work_units[k / p.h_q];
+    const int n = min(u.y, *p.work_count - u.x);
+    return PairUnit{u.x, n > 0 ? n : 0, k % p.h_q};
+  } else {
+    return PairUnit{k, 1, 0};
+  }
+}
+
+// Item k of the launch (jagged: worklist item k for head h).  Dense / partial
+// items: the Q tiles of one head (pair) and batch are consecutive, longest
+// causal walk first, so the CTAs that run at one time share the K/V of one
+// head in L2.
+template <int kMode>
+__device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int k, int h) {
   constexpr int BM = 128;
   PairItem it;
   if constexpr (kMode == kModeJagged) {
-    const int4 w = p.work_items[k / p.h_q];  // a 256-row Q tile of one sequence
-    const int h = k % p.h_q;
+    const int4 w = p.work_items[k];  // a 256-row Q tile of one sequence
     const int a_hi = w.z + min(w.w, BM);
     it.b = 0;
     it.st0 = SubTile{h, w.z, a_hi};
@@ -100,6 +120,7 @@ __device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int k) {
     it.q_pos0 = 0;
     it.kv_pos0 = 0;
   } else {
+    (void)h;
     const int yb = k / p.n_qt;
     const int t_rank = k - yb * p.n_qt;
     const int y = yb % p.n_y;
@@ -227,33 +248,39 @@ __global__ void __launch_bounds__(352, 1)
       for (int r = 0; ok && (kPersistent || r == 0); ++r) {
         const int k = pair_item_index(r, total);
         if (k < 0) break;
-        const PairItem it = pair_item<kMode>(p, k);
-        TileWalk walk;
-        const int n = item_walk(it, walk);
-        if (n == 0) continue;
-        const int hk = it.st0.h / p.group;
-        // Q once the previous item's MMAs are done with the Q buffer, then
-        // K/V in the MMA's first-use order: K(0), and per tile V(j), K(j+1)
-        TileWalk kw = walk, vw = walk;
-        int ch, s0, me;
-        if (q_loads > 0 && !pf_wait(&bar_qe, (uint32_t)((q_loads - 1) & 1), &abort_flag, 4)) break;
-        const int nq = it.st1.empty() ? 1 : 2;
-        mbar_arrive_expect_tx(&bar_q, nq * C::Q_BYTES);
-        for (int x = 0; x < nq; ++x) {
-          const SubTile t = x ? it.st1 : it.st0;
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, t.h, t.q_lo, it.b);
-        }
-        ++q_loads;
-        kw.next(ch, s0, me);
-        ok = push(&mk, hk, s0, it.b);
-        if (!ok) break;
-        for (int j = 0; ok && j < n; ++j) {
-          vw.next(ch, s0, me);
-          ok = push(&mv, hk, s0, it.b);
-          if (ok && j + 1 < n) {
-            kw.next(ch, s0, me);
-            ok = push(&mk, hk, s0, it.b);
+        const PairUnit un = pair_unit<kMode>(p, k);
+        for (int ii = 0; ok && ii < un.n; ++ii) {
+          const PairItem it = pair_item<kMode>(p, un.i0 + ii, un.h);
+          TileWalk walk;
+          const int n = item_walk(it, walk);
+          if (n == 0) continue;
+          const int hk = it.st0.h / p.group;
+          // Q once the previous item's MMAs are done with the Q buffer, then
+          // K/V in the MMA's first-use order: K(0), and per tile V(j), K(j+1)
+          TileWalk kw = walk, vw = walk;
+          int ch, s0, me;
+          if (q_loads > 0 && !pf_wait(&bar_qe, (uint32_t)((q_loads - 1) & 1), &abort_flag, 4)) {
+            ok = false;
+            break;
+          }
+          const int nq = it.st1.empty() ? 1 : 2;
+          mbar_arrive_expect_tx(&bar_q, nq * C::Q_BYTES);
+          for (int x = 0; x < nq; ++x) {
+            const SubTile t = x ? it.st1 : it.st0;
+            for (int blk = 0; blk < D / 64; ++blk)
+              tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, t.h, t.q_lo, it.b);
+          }
+          ++q_loads;
+          kw.next(ch, s0, me);
+          ok = push(&mk, hk, s0, it.b);
+          if (!ok) break;
+          for (int j = 0; ok && j < n; ++j) {
+            vw.next(ch, s0, me);
+            ok = push(&mv, hk, s0, it.b);
+            if (ok && j + 1 < n) {
+              kw.next(ch, s0, me);
+              ok = push(&mk, hk, s0, it.b);
+            }
           }
         }
       }
@@ -295,70 +322,76 @@ __global__ void __launch_bounds__(352, 1)
       for (int r = 0; ok && (kPersistent || r == 0); ++r) {
         const int k = pair_item_index(r, total);
         if (k < 0) break;
-        const PairItem it = pair_item<kMode>(p, k);
-        TileWalk walk;
-        const int n = item_walk(it, walk);
-        if (n == 0) continue;
-        if (s_role) {
-          if (!pf_wait(&bar_q, (uint32_t)(q_items & 1), &abort_flag, 5)) break;
-          tc_fence_after_sync();
-          ++q_items;
-        }
-        bool acc[2] = {false, false};  // O_x already holds this item's sum
-        for (int j = 0; ok && j < n; ++j) {
-          int ch, kstart, me;
-          walk.next(ch, kstart, me);
-          const bool act[2] = {active(it, 0, kstart), active(it, 1, kstart)};
-          const int slab = slab0 + 2 * j + (s_role ? 0 : 1);  // K(j) or V(j)
-          ok = wait_slab(slab);
-          if (!ok) break;
-          const uint32_t stage_addr = skv + (slab % C::NST) * C::SLAB_BYTES;
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!act[x]) continue;
-            const bool last = x == 1 || !act[1];  // last reader of the stage
-            if (s_role) {
-              if (groups[x] > 0) {
-                // the sub-tile's previous P.V has read its P
-                ok = pf_wait(&bar_o[x], (uint32_t)((groups[x] - 1) & 1), &abort_flag, 11);
+        const PairUnit un = pair_unit<kMode>(p, k);
+        for (int ii = 0; ok && ii < un.n; ++ii) {
+          const PairItem it = pair_item<kMode>(p, un.i0 + ii, un.h);
+          TileWalk walk;
+          const int n = item_walk(it, walk);
+          if (n == 0) continue;
+          if (s_role) {
+            if (!pf_wait(&bar_q, (uint32_t)(q_items & 1), &abort_flag, 5)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            ++q_items;
+          }
+          bool acc[2] = {false, false};  // O_x already holds this item's sum
+          for (int j = 0; ok && j < n; ++j) {
+            int ch, kstart, me;
+            walk.next(ch, kstart, me);
+            const bool act[2] = {active(it, 0, kstart), active(it, 1, kstart)};
+            const int slab = slab0 + 2 * j + (s_role ? 0 : 1);  // K(j) or V(j)
+            ok = wait_slab(slab);
+            if (!ok) break;
+            const uint32_t stage_addr = skv + (slab % C::NST) * C::SLAB_BYTES;
+  #pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              if (!act[x]) continue;
+              const bool last = x == 1 || !act[1];  // last reader of the stage
+              if (s_role) {
+                if (groups[x] > 0) {
+                  // the sub-tile's previous P.V has read its P
+                  ok = pf_wait(&bar_o[x], (uint32_t)((groups[x] - 1) & 1), &abort_flag, 11);
+                  if (!ok) break;
+                  tc_fence_after_sync();
+                }
+                const uint64_t kdesc = smem_desc_sw128(stage_addr, 16, 1024);
+                const uint64_t qdesc = smem_desc_sw128(sq + x * C::Q_BYTES, 16, 1024);
+                const uint32_t s_tmem = tmem + static_cast<uint32_t>(x * 128);
+                // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle
+                // row, the next 64-column block every four steps
+  #pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                  const uint32_t off = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+                  mma_ss(s_tmem, desc_advance(qdesc, off), desc_advance(kdesc, off), kIdescS, ks != 0);
+                }
+                if (last) mma_commit(&bar_empty[slab % C::NST]);
+                mma_commit(&bar_s[x]);
+              } else {
+                ok = pf_wait(&bar_p[x], (uint32_t)(groups[x] & 1), &abort_flag, 3);
                 if (!ok) break;
                 tc_fence_after_sync();
+                const uint64_t vdesc = smem_desc_sw128(stage_addr, 16384, 1024);
+                const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
+                const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(x * D);
+                // 16 keys of V (16 rows of 256 bytes, two swizzle atoms) per MMA
+  #pragma unroll
+                for (int ks = 0; ks < C::BN / 16; ++ks)
+                  mma_ts(o_tmem, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                         (ks > 0 || acc[x]) ? 1u : 0u);
+                acc[x] = true;
+                if (last) mma_commit(&bar_empty[slab % C::NST]);
+                mma_commit(&bar_o[x]);
               }
-              const uint64_t kdesc = smem_desc_sw128(stage_addr, 16, 1024);
-              const uint64_t qdesc = smem_desc_sw128(sq + x * C::Q_BYTES, 16, 1024);
-              const uint32_t s_tmem = tmem + static_cast<uint32_t>(x * 128);
-              // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle
-              // row, the next 64-column block every four steps
-#pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-                mma_ss(s_tmem, desc_advance(qdesc, off), desc_advance(kdesc, off), kIdescS, ks != 0);
-              }
-              if (last) mma_commit(&bar_empty[slab % C::NST]);
-              mma_commit(&bar_s[x]);
-            } else {
-              ok = pf_wait(&bar_p[x], (uint32_t)(groups[x] & 1), &abort_flag, 3);
-              if (!ok) break;
-              tc_fence_after_sync();
-              const uint64_t vdesc = smem_desc_sw128(stage_addr, 16384, 1024);
-              const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
-              const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(x * D);
-              // 16 keys of V (16 rows of 256 bytes, two swizzle atoms) per MMA
-#pragma unroll
-              for (int ks = 0; ks < C::BN / 16; ++ks)
-                mma_ts(o_tmem, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
-                       (ks > 0 || acc[x]) ? 1u : 0u);
-              acc[x] = true;
-              if (last) mma_commit(&bar_empty[slab % C::NST]);
-              mma_commit(&bar_o[x]);
+              ++groups[x];
             }
-            ++groups[x];
           }
+          if (!ok) break;
+          // the item's S MMAs, the last readers of its Q, release the Q buffer
+          if (s_role) mma_commit(&bar_qe);
+          slab0 += 2 * n;
         }
-        if (!ok) break;
-        // the item's S MMAs, the last readers of its Q, release the Q buffer
-        if (s_role) mma_commit(&bar_qe);
-        slab0 += 2 * n;
       }
       // every MMA either issuer issued must finish before TMEM is released
       mma_commit(&bar_fin);
@@ -380,201 +413,207 @@ __global__ void __launch_bounds__(352, 1)
     for (int r = 0; ok && (kPersistent || r == 0); ++r) {
       const int k = pair_item_index(r, total);
       if (k < 0) break;
-      const PairItem it = pair_item<kMode>(p, k);
-      TileWalk walk;
-      const int n = item_walk(it, walk);
-      const SubTile me_t = x ? it.st1 : it.st0;
-      const int q_row = me_t.q_lo + row;
-      float m_run = -CUDART_INF_F;  // reference max (exp2 domain), raised lazily
-      float l_run = 0.f;            // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
-      float lr_run = 0.f;           // sum of the rounded P the MMA multiplies V by: normalises O
-      float m_max = -CUDART_INF_F;  // true running max (partial mode)
-      int cnt_item = 0;             // tiles of this item this sub-tile took part in
-      for (int j = 0; j < n; ++j) {
-        int ch, kstart, mend;
-        walk.next(ch, kstart, mend);
-        if (!active(it, x, kstart)) continue;
-        if (!pf_wait(&bar_s[x], (uint32_t)(cnt & 1), &abort_flag, 6)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // S_x(j) was issued after this sub-tile's previous P.V by the same
-        // thread, so its completion also means that P.V has finished: O may
-        // be rescaled without waiting on bar_o.
-        constexpr bool win = kMode == kModeWindow;
-        const bool need_mask =
-            (kstart + C::BN > mend) ||
-            (p.causal && ((long long)it.kv_pos0 + kstart + C::BN - 1 > (long long)it.q_pos0 + me_t.q_lo)) ||
-            (win && (long long)it.kv_pos0 + kstart < (long long)it.q_pos0 + me_t.q_hi - 1 - p.window);
-        long long lim = C::BN;  // key kstart + i is visible iff flo <= i < lim
-        long long flo = 0;
-        if (need_mask) {
-          lim = (long long)mend - kstart;
-          if (p.causal) {
-            const long long lc = (long long)it.q_pos0 + q_row - it.kv_pos0 - kstart + 1;
-            lim = lc < lim ? lc : lim;
-            if (win) flo = lc - 1 - p.window;
+      const PairUnit un = pair_unit<kMode>(p, k);
+      for (int ii = 0; ok && ii < un.n; ++ii) {
+        const PairItem it = pair_item<kMode>(p, un.i0 + ii, un.h);
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        const SubTile me_t = x ? it.st1 : it.st0;
+        const int q_row = me_t.q_lo + row;
+        float m_run = -CUDART_INF_F;  // reference max (exp2 domain), raised lazily
+        float l_run = 0.f;            // sum of exp2(x - m_run) in fp32: the triplet's l and the LSE
+        float lr_run = 0.f;           // sum of the rounded P the MMA multiplies V by: normalises O
+        float m_max = -CUDART_INF_F;  // true running max (partial mode)
+        int cnt_item = 0;             // tiles of this item this sub-tile took part in
+        for (int j = 0; j < n; ++j) {
+          int ch, kstart, mend;
+          walk.next(ch, kstart, mend);
+          if (!active(it, x, kstart)) continue;
+          if (!pf_wait(&bar_s[x], (uint32_t)(cnt & 1), &abort_flag, 6)) {
+            ok = false;
+            break;
           }
-        }
-        // the first 64 columns are reduced while the second pair of loads is in flight
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(scol, r0);
-        tmem_ld32(scol + 32, r1);
-        tmem_ld_wait(r0);
-        tmem_ld_wait(r1);
-        tmem_ld32(scol + 64, r2);
-        tmem_ld32(scol + 96, r3);
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i >= lim || i < flo) r0[i] = ninf;
-            if (i + 32 >= lim || i + 32 < flo) r1[i] = ninf;
+          tc_fence_after_sync();
+          // S_x(j) was issued after this sub-tile's previous P.V by the same
+          // thread, so its completion also means that P.V has finished: O may
+          // be rescaled without waiting on bar_o.
+          constexpr bool win = kMode == kModeWindow;
+          const bool need_mask =
+              (kstart + C::BN > mend) ||
+              (p.causal && ((long long)it.kv_pos0 + kstart + C::BN - 1 > (long long)it.q_pos0 + me_t.q_lo)) ||
+              (win && (long long)it.kv_pos0 + kstart < (long long)it.q_pos0 + me_t.q_hi - 1 - p.window);
+          long long lim = C::BN;  // key kstart + i is visible iff flo <= i < lim
+          long long flo = 0;
+          if (need_mask) {
+            lim = (long long)mend - kstart;
+            if (p.causal) {
+              const long long lc = (long long)it.q_pos0 + q_row - it.kv_pos0 - kstart + 1;
+              lim = lc < lim ? lc : lim;
+              if (win) flo = lc - 1 - p.window;
+            }
           }
-        }
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          mx8[i] = fmax3(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8]), __uint_as_float(r0[i + 16]));
-          mx8[i] = fmax3(mx8[i], __uint_as_float(r0[i + 24]), __uint_as_float(r1[i]));
-          mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 8]), __uint_as_float(r1[i + 16]));
-        }
-        tmem_ld_wait(r2);
-        tmem_ld_wait(r3);
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i + 64 >= lim || i + 64 < flo) r2[i] = ninf;
-            if (i + 96 >= lim || i + 96 < flo) r3[i] = ninf;
+          // the first 64 columns are reduced while the second pair of loads is in flight
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(scol, r0);
+          tmem_ld32(scol + 32, r1);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
+          tmem_ld32(scol + 64, r2);
+          tmem_ld32(scol + 96, r3);
+          if (need_mask) {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i >= lim || i < flo) r0[i] = ninf;
+              if (i + 32 >= lim || i + 32 < flo) r1[i] = ninf;
+            }
           }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 24]), __uint_as_float(r2[i]));
-          mx8[i] = fmax3(mx8[i], __uint_as_float(r2[i + 8]), __uint_as_float(r2[i + 16]));
-          mx8[i] = fmax3(mx8[i], __uint_as_float(r2[i + 24]), __uint_as_float(r3[i]));
-          mx8[i] = fmax3(mx8[i], __uint_as_float(r3[i + 8]), __uint_as_float(r3[i + 16]));
-          mx8[i] = fmaxf(mx8[i], __uint_as_float(r3[i + 24]));
-        }
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-        const float m_tile = mx * c;  // -inf when the whole row is masked
-        if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
-        const float m_new = fmaxf(m_run, m_tile);
-        const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
-        float alpha = 1.f;
-        if (raise) {
-          alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
-          m_run = m_new;
-          l_run *= alpha;
-          lr_run *= alpha;
-        }
-        const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
-        const uint64_t nm2 = f2_make(neg_m, neg_m);
-        uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
-        uint32_t pk[16];
-        auto pack_chunk = [&](uint32_t (&rr)[32], uint32_t col) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 e = f2_split(f2_fma(f2_make_u(rr[2 * i], rr[2 * i + 1]), c2, nm2));
-            const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
-            pk[i] = pack_half2<kBf16>(p0, p1);
-            sum2 = f2_add(sum2, f2_make(p0, p1));
-            // O is normalised by the sum of the rounded weights it was built
-            // from, so O / l is a weighted mean with consistent weights
-            const float2 pr = unpack_half2<kBf16>(pk[i]);
-            sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
+          float mx8[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            mx8[i] = fmax3(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8]), __uint_as_float(r0[i + 16]));
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r0[i + 24]), __uint_as_float(r1[i]));
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 8]), __uint_as_float(r1[i + 16]));
           }
-          tmem_st16(scol + col, pk);
-        };
-        // P overwrites the first 64 columns of S, already in registers
-        pack_chunk(r0, 0);
-        pack_chunk(r1, 16);
-        // O (complete up to the previous tile, see above) is rescaled before
-        // P(j) is published
-        if (cnt_item > 0 && __any_sync(0xffffffffu, raise)) {
-#pragma unroll 1
+          tmem_ld_wait(r2);
+          tmem_ld_wait(r3);
+          if (need_mask) {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i + 64 >= lim || i + 64 < flo) r2[i] = ninf;
+              if (i + 96 >= lim || i + 96 < flo) r3[i] = ninf;
+            }
+          }
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 24]), __uint_as_float(r2[i]));
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r2[i + 8]), __uint_as_float(r2[i + 16]));
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r2[i + 24]), __uint_as_float(r3[i]));
+            mx8[i] = fmax3(mx8[i], __uint_as_float(r3[i + 8]), __uint_as_float(r3[i + 16]));
+            mx8[i] = fmaxf(mx8[i], __uint_as_float(r3[i + 24]));
+          }
+          const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+          const float m_tile = mx * c;  // -inf when the whole row is masked
+          if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
+          const float m_new = fmaxf(m_run, m_tile);
+          const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
+          float alpha = 1.f;
+          if (raise) {
+            alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
+            m_run = m_new;
+            l_run *= alpha;
+            lr_run *= alpha;
+          }
+          const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+          const uint64_t nm2 = f2_make(neg_m, neg_m);
+          uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
+          uint32_t pk[16];
+          auto pack_chunk = [&](uint32_t (&rr)[32], uint32_t col) {
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 e = f2_split(f2_fma(f2_make_u(rr[2 * i], rr[2 * i + 1]), c2, nm2));
+              const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+              pk[i] = pack_half2<kBf16>(p0, p1);
+              sum2 = f2_add(sum2, f2_make(p0, p1));
+              // O is normalised by the sum of the rounded weights it was built
+              // from, so O / l is a weighted mean with consistent weights
+              const float2 pr = unpack_half2<kBf16>(pk[i]);
+              sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
+            }
+            tmem_st16(scol + col, pk);
+          };
+          // P overwrites the first 64 columns of S, already in registers
+          pack_chunk(r0, 0);
+          pack_chunk(r1, 16);
+          // O (complete up to the previous tile, see above) is rescaled before
+          // P(j) is published
+          if (cnt_item > 0 && __any_sync(0xffffffffu, raise)) {
+  #pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(ocol + cc * 32, o);
+              tmem_ld_wait(o);
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(ocol + cc * 32, o);
+            }
+          }
+          pack_chunk(r2, 32);
+          pack_chunk(r3, 48);
+          const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
+          l_run += sv.x + sv.y;
+          lr_run += srv.x + srv.y;
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&bar_p[x]);
+          ++cnt;
+          ++cnt_item;
+        }
+        if (!ok) break;
+        if (cnt_item > 0) {
+          // the item's last P.V of this sub-tile (earlier ones are done, see above)
+          if (!pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 8)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        const bool row_valid = q_row < me_t.q_hi;
+        const size_t row_idx = ((size_t)it.b * p.S_q + q_row) * p.h_q + me_t.h;
+        const size_t lse_idx = ((size_t)it.b * p.h_q + me_t.h) * p.S_q + q_row;
+        constexpr float kLn2 = 0.693147180559945309f;
+        if constexpr (kMode != kModePartial) {
+          const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D;
+  #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld32(ocol + cc * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(ocol + cc * 32, o);
+            if (cnt_item > 0) {
+              tmem_ld32(ocol + cc * 32, o);
+              tmem_ld_wait(o);
+            } else {
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            uint32_t w[16];
+  #pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (row_valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+  #pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+            }
           }
-        }
-        pack_chunk(r2, 32);
-        pack_chunk(r3, 48);
-        const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
-        l_run += sv.x + sv.y;
-        lr_run += srv.x + srv.y;
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&bar_p[x]);
-        ++cnt;
-        ++cnt_item;
-      }
-      if (!ok) break;
-      if (cnt_item > 0) {
-        // the item's last P.V of this sub-tile (earlier ones are done, see above)
-        if (!pf_wait(&bar_o[x], (uint32_t)((cnt - 1) & 1), &abort_flag, 8)) break;
-        tc_fence_after_sync();
-      }
-      const bool row_valid = q_row < me_t.q_hi;
-      const size_t row_idx = ((size_t)it.b * p.S_q + q_row) * p.h_q + me_t.h;
-      const size_t lse_idx = ((size_t)it.b * p.h_q + me_t.h) * p.S_q + q_row;
-      constexpr float kLn2 = 0.693147180559945309f;
-      if constexpr (kMode != kModePartial) {
-        const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
-        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          if (cnt_item > 0) {
-            tmem_ld32(ocol + cc * 32, o);
-            tmem_ld_wait(o);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-          }
-        }
-        if (p.lse != nullptr && row_valid)
-          p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
-      } else {
-        const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
-        const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
-        // O re-weighted so that O / l equals the consistently normalised O_acc / lr
-        const float fo = any ? f * (l_run / lr_run) : 0.f;
-        float* orow = p.o_part + row_idx * D;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          if (cnt_item > 0) {
-            tmem_ld32(ocol + cc * 32, o);
-            tmem_ld_wait(o);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          if (p.lse != nullptr && row_valid)
+            p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
+        } else {
+          const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
+          const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
+          // O re-weighted so that O / l equals the consistently normalised O_acc / lr
+          const float fo = any ? f * (l_run / lr_run) : 0.f;
+          float* orow = p.o_part + row_idx * D;
+  #pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            if (cnt_item > 0) {
+              tmem_ld32(ocol + cc * 32, o);
+              tmem_ld_wait(o);
+            } else {
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            if (row_valid) {
+              float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+  #pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
+                                      __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+            }
           }
           if (row_valid) {
-            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
-                                    __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+            p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
+            p.l_out[lse_idx] = any ? l_run * f : 0.f;
           }
-        }
-        if (row_valid) {
-          p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
-          p.l_out[lse_idx] = any ? l_run * f : 0.f;
         }
       }
     }

@@ -14,7 +14,14 @@
 // tile has the longest causal KV walk).  When ceil(max_seqlen / block_m) > 64
 // the count buckets are skipped and sequences stay in index order.
 //
-// Output buffer: int count at word 0, items from byte 16.
+// Units ("Grouping" on the same page: successive Q work items of one sequence
+// reuse its resident K/V range): one int2 {first_item, n_items} per sequence
+// with at least one tile, in the same order; a persistent kernel takes a unit
+// and one head at a time, so the sequence's tiles run back to back on one SM
+// and its K/V is re-read from L2 rather than HBM.
+//
+// Output buffer: int item count at word 0, int unit count at word 1, items
+// from byte 16 (max_items of them), then the units.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -26,8 +33,9 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
                                                         int total_tokens, int max_seqlen, int block_m,
                                                         int* __restrict__ out, int max_items) {
   int4* items = reinterpret_cast<int4*>(out + 4);
-  __shared__ int warp_sums[32];
-  __shared__ int s_base;
+  int2* units = reinterpret_cast<int2*>(out + 4 + 4 * (size_t)max_items);
+  __shared__ long long warp_sums[32];
+  __shared__ int s_base, s_ubase;
   __shared__ int s_bad;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -36,6 +44,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
   const bool bucketed = nmax <= 64;
   if (tid == 0) {
     s_base = 0;
+    s_ubase = 0;
     s_bad = 0;
   }
   __syncthreads();
@@ -57,28 +66,30 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
       }
       const bool take = bucketed ? (nt == want && nt > 0) : (nt > 0);
       const int cnt = take ? nt : 0;
-      // block-wide exclusive scan of cnt
-      int x = cnt;
+      // block-wide exclusive scan of (tiles << 32) | units, both counts < 2^31
+      const long long v = ((long long)cnt << 32) | (take ? 1 : 0);
+      long long x = v;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, d);
+        const long long y = __shfl_up_sync(0xffffffffu, x, d);
         if (lane >= d) x += y;
       }
       if (lane == 31) warp_sums[w] = x;
       __syncthreads();
       if (w == 0) {
-        int y = warp_sums[lane];
+        long long y = warp_sums[lane];
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-          const int z = __shfl_up_sync(0xffffffffu, y, d);
+          const long long z = __shfl_up_sync(0xffffffffu, y, d);
           if (lane >= d) y += z;
         }
         warp_sums[lane] = y;
       }
       __syncthreads();
-      const int excl = x - cnt + (w > 0 ? warp_sums[w - 1] : 0);
-      const int total = warp_sums[31];
-      const int base = s_base;
+      const long long ex = x - v + (w > 0 ? warp_sums[w - 1] : 0);
+      const int excl = (int)(ex >> 32), uexcl = (int)(ex & 0xffffffffLL);
+      const int total = (int)(warp_sums[31] >> 32), utotal = (int)(warp_sums[31] & 0xffffffffLL);
+      const int base = s_base, ubase = s_ubase;
       if (take) {
         for (int t = 0; t < nt; ++t) {
           const long long pos = (long long)base + excl + (nt - 1 - t);
@@ -88,15 +99,20 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
             items[pos] = make_int4(begin, len, tile_start, extent);
           }
         }
+        units[ubase + uexcl] = make_int2(base + excl, nt);  // ubase + uexcl < num_seqs
       }
       __syncthreads();
-      if (tid == 0) s_base = base + total;
+      if (tid == 0) {
+        s_base = base + total;
+        s_ubase = ubase + utotal;
+      }
       __syncthreads();
     }
   }
   if (tid == 0) {
     const int count = s_base < max_items ? s_base : max_items;
     out[0] = count;
+    out[1] = s_ubase;  // consumers skip unit items at or beyond out[0]
     if (s_bad || s_base > max_items) atomicOr(&g_worklist_status, kStatusDeviceInput);
   }
 }

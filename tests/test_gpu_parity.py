@@ -257,6 +257,18 @@ def test_jagged_parity_and_worklist(causal, D):
     for a, b in zip(items, items[1:]):
         if a[0] == b[0]:
             assert b[2] == a[2] - block_m
+    # units: one per non-empty sequence, covering its contiguous items in order
+    n_units = int(words[1])
+    max_items = (int(offs[-1]) + (len(offs) - 1) * (block_m - 1)) // block_m
+    units = words[4 + 4 * max_items:4 + 4 * max_items + 2 * n_units].reshape(n_units, 2)
+    assert n_units == sum(1 for L in lengths if L > 0)
+    assert units[0][0] == 0 and all(u[1] >= 1 for u in units)
+    for u, u2 in zip(units, units[1:]):
+        assert u2[0] == u[0] + u[1]
+    assert units[-1][0] + units[-1][1] == count
+    for u in units:
+        seq = items[u[0]:u[0] + u[1]]
+        assert all(r[0] == seq[0][0] for r in seq) and u[1] == (seq[0][1] + block_m - 1) // block_m
 
 
 def test_jagged_random_lengths():
