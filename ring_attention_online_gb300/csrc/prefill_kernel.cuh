@@ -210,11 +210,10 @@ __global__ void __launch_bounds__(352, 1)
       // except V(n - 1), the last tile, 2n - 1
       auto k_tile = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
       auto v_tile = [&](int j) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; };
-      auto wait_slabs = [&](int tile, uint32_t site) -> bool {
-        for (int hs = 0; hs < C::NH; ++hs) {
-          const int s = tile * C::NH + hs;
-          if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, site)) return false;
-        }
+      // each slab is waited for right before its MMAs, so the first half of S(j)
+      // (PV(j)) can run while the second half's K (V) is still landing
+      auto wait_slab = [&](int s, uint32_t site) -> bool {
+        if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, site)) return false;
         tc_fence_after_sync();
         return true;
       };
@@ -230,11 +229,11 @@ __global__ void __launch_bounds__(352, 1)
             tc_fence_after_sync();
           }
           const int kt = k_tile(j);
-          ok = wait_slabs(kt, 2);
-          if (!ok) break;
           const uint32_t d_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
           for (int hs = 0; hs < C::NH; ++hs) {
             const int stage = (kt * C::NH + hs) % C::NST;
+            ok = wait_slab(kt * C::NH + hs, 2);
+            if (!ok) break;
             const uint64_t kdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < C::SC / 16; ++ks) {
@@ -244,6 +243,7 @@ __global__ void __launch_bounds__(352, 1)
             }
             mma_commit(&bar_empty[stage]);
           }
+          if (!ok) break;
           mma_commit(&bar_s[j & 1]);
         }
       } else {
@@ -251,12 +251,13 @@ __global__ void __launch_bounds__(352, 1)
           ok = pf_wait(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3);
           if (!ok) break;
           const int vt = v_tile(j);
-          ok = wait_slabs(vt, 4);
-          if (!ok) break;
+          tc_fence_after_sync();  // P(j) in TMEM
           const uint32_t p_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
           for (int hs = 0; hs < C::NH; ++hs) {
             const int stage = (vt * C::NH + hs) % C::NST;
+            ok = wait_slab(vt * C::NH + hs, 4);
+            if (!ok) break;
             const uint64_t vdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16384, 1024);
 #pragma unroll
             for (int ks = 0; ks < C::BN / 16; ++ks)
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(352, 1)
                      ks > 0 ? 1u : acc0);
             mma_commit(&bar_empty[stage]);
           }
+          if (!ok) break;
           mma_commit(&bar_o[j & 1]);
         }
       }
