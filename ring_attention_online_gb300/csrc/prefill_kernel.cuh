@@ -52,7 +52,9 @@ struct PrefillCfg {
   static constexpr int NST = D == 64 ? 8 : 4;
   static constexpr int SMEM_BYTES = Q_BYTES + NST * SLAB_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  // S(j) / P(j) live in TMEM columns [128*(j%2), 128*(j%2)+128); O after them
+  // TMEM: S(j) in columns [0, 128) (one buffer); P(j) (bf16/fp16, 64 columns)
+  // in [P_COL + 64*(j%2), +64); O in [O_COL, O_COL + D)
+  static constexpr uint32_t P_COL = 128;
   static constexpr uint32_t O_COL = 256;
   static constexpr int THREADS = 352;  // TMA warp, S issuer, 8 softmax warps, PV issuer
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
@@ -71,6 +73,7 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2]
   __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
   __shared__ uint64_t bar_s[2], bar_p[2];
+  __shared__ uint64_t bar_sfree[2];  // the softmax warps have read S(j) out of TMEM (j % 2)
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
   __shared__ float xch_max[2][2][128];  // [tile parity][column half][row]
@@ -127,6 +130,7 @@ __global__ void __launch_bounds__(352, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_sfree[i], 256);
       mbar_init(&bar_p[i], 256);
       for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 64);
     }
@@ -223,13 +227,14 @@ __global__ void __launch_bounds__(352, 1)
         ok = pf_wait(&bar_q, 0, &abort_flag, 5);
         tc_fence_after_sync();
         for (int j = 0; ok && j < n; ++j) {
-          if (j >= 2) {
-            ok = pf_wait(&bar_o[j & 1], (uint32_t)(((j - 2) >> 1) & 1), &abort_flag, 11);
+          if (j >= 1) {
+            // the one S buffer is free once the softmax warps have read S(j-1)
+            ok = pf_wait(&bar_sfree[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 11);
             if (!ok) break;
             tc_fence_after_sync();
           }
           const int kt = k_tile(j);
-          const uint32_t d_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+          const uint32_t d_tmem = tmem;
           for (int hs = 0; hs < C::NH; ++hs) {
             const int stage = (kt * C::NH + hs) % C::NST;
             ok = wait_slab(kt * C::NH + hs, 2);
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(352, 1)
           if (!ok) break;
           const int vt = v_tile(j);
           tc_fence_after_sync();  // P(j) in TMEM
-          const uint32_t p_tmem = tmem + static_cast<uint32_t>((j & 1) * 128);
+          const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((j & 1) * 64);
           const uint32_t acc0 = j > 0 ? 1u : 0u;
           for (int hs = 0; hs < C::NH; ++hs) {
             const int stage = (vt * C::NH + hs) % C::NST;
@@ -302,12 +307,14 @@ __global__ void __launch_bounds__(352, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint32_t scol = lane_addr + static_cast<uint32_t>(buf * 128);
       uint32_t r0[32], r1[32];
-      tmem_ld32(scol + half * 64, r0);
-      tmem_ld32(scol + half * 64 + 32, r1);
+      tmem_ld32(lane_addr + half * 64, r0);
+      tmem_ld32(lane_addr + half * 64 + 32, r1);
       tmem_ld_wait(r0);
       tmem_ld_wait(r1);
+      // S(j) is in registers: the S issuer may overwrite the buffer with S(j+1)
+      tc_fence_before_sync();
+      mbar_arrive(&bar_sfree[buf]);
 
       // mask the diagonal / tail tile (key kstart + i is visible iff i < lim)
       // and, under a sliding window, the tiles at its lower edge (iff i >= flo)
@@ -341,8 +348,7 @@ __global__ void __launch_bounds__(352, 1)
         mx8[i] = fmaxf(mx8[i], __uint_as_float(r1[i + 24]));
       }
       float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      // both halves of the row see each other's max (the S(j) columns are all in
-      // registers by now, so P may overwrite them after this barrier)
+      // both halves of the row see each other's max
       xch_max[buf][half][row] = mx;
       mbar_arrive(&bar_x[buf][wq]);
       if (!pf_wait(&bar_x[buf][wq], (uint32_t)((j >> 1) & 1), &abort_flag, 9)) {
@@ -361,6 +367,17 @@ __global__ void __launch_bounds__(352, 1)
         l_run *= alpha;
         lr_run *= alpha;
       }
+      // P(j) goes to P buffer j % 2, which PV(j-2) read; PV(j-2) is waited for
+      // here and so always before PV(j) is issued (no waiter falls two phases
+      // behind on bar_o)
+      if (j >= 2) {
+        if (!pf_wait(&bar_o[buf], (uint32_t)(((j - 2) >> 1) & 1), &abort_flag, 12)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+      }
+      const uint32_t pcol = lane_addr + C::P_COL + static_cast<uint32_t>(buf * 64);
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
       const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
       uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
@@ -377,9 +394,9 @@ __global__ void __launch_bounds__(352, 1)
           const float2 pr = unpack_half2<kBf16>(pk[i]);
           sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
         }
-        tmem_st16(scol + col, pk);
+        tmem_st16(pcol + col, pk);
       };
-      // P(j) for keys [64*half, 64*half+64) goes to columns [32*half, 32*half+32)
+      // P(j) for keys [64*half, 64*half+64) goes to its columns [32*half, 32*half+32)
       pack_chunk(r0, half * 32);
       pack_chunk(r1, half * 32 + 16);
       const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
@@ -387,10 +404,9 @@ __global__ void __launch_bounds__(352, 1)
       lr_run += srv.x + srv.y;
 
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        // PV(j-1) must be complete before O is rescaled.  PV(j-2) is (S(j) was
-        // issued after it), so with P.V groups alternating between two
-        // barriers this wait is never more than one phase behind, and the
-        // tiles that need no rescale need not wait at all.
+        // PV(j-1) must be complete before O is rescaled.  PV(j-3), on the same
+        // barrier, was waited for above one tile ago, so this wait is never more
+        // than one phase behind, and tiles that need no rescale need not wait.
         if (!pf_wait(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 7)) {
           ok = false;
           break;
