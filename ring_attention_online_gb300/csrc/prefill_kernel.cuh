@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(352, 1)
       bool ok = true;
       auto push = [&](const CUtensorMap* map, int start) -> bool {
         for (int hs = 0; hs < C::NH; ++hs) {
-          if (!pf_wait(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
+          if (!pf_wait_outlined(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
           uint8_t* dst = sKV + stage * C::SLAB_BYTES;
           mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
           for (int blk = 0; blk < C::BLK_PER_SLAB; ++blk)
@@ -217,19 +217,19 @@ __global__ void __launch_bounds__(352, 1)
       // each slab is waited for right before its MMAs, so the first half of S(j)
       // (PV(j)) can run while the second half's K (V) is still landing
       auto wait_slab = [&](int s, uint32_t site) -> bool {
-        if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, site)) return false;
+        if (!pf_wait_outlined(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, site)) return false;
         tc_fence_after_sync();
         return true;
       };
       bool ok = true;
       if (warp == 1) {
         const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-        ok = pf_wait(&bar_q, 0, &abort_flag, 5);
+        ok = pf_wait_outlined(&bar_q, 0, &abort_flag, 5);
         tc_fence_after_sync();
         for (int j = 0; ok && j < n; ++j) {
           if (j >= 1) {
             // the one S buffer is free once the softmax warps have read S(j-1)
-            ok = pf_wait(&bar_sfree[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 11);
+            ok = pf_wait_outlined(&bar_sfree[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 11);
             if (!ok) break;
             tc_fence_after_sync();
           }
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(352, 1)
         }
       } else {
         for (int j = 0; ok && j < n; ++j) {
-          ok = pf_wait(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3);
+          ok = pf_wait_outlined(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3);
           if (!ok) break;
           const int vt = v_tile(j);
           tc_fence_after_sync();  // P(j) in TMEM
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(352, 1)
       int ch, kstart, mend;
       sw_walk.next(ch, kstart, mend);
       const int buf = j & 1;
-      if (!pf_wait(&bar_s[buf], (uint32_t)((j >> 1) & 1), &abort_flag, 6)) {
+      if (!pf_wait_outlined(&bar_s[buf], (uint32_t)((j >> 1) & 1), &abort_flag, 6)) {
         ok = false;
         break;
       }
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(352, 1)
       // both halves of the row see each other's max
       xch_max[buf][half][row] = mx;
       mbar_arrive(&bar_x[buf][wq]);
-      if (!pf_wait(&bar_x[buf][wq], (uint32_t)((j >> 1) & 1), &abort_flag, 9)) {
+      if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((j >> 1) & 1), &abort_flag, 9)) {
         ok = false;
         break;
       }
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(352, 1)
       // here and so always before PV(j) is issued (no waiter falls two phases
       // behind on bar_o)
       if (j >= 2) {
-        if (!pf_wait(&bar_o[buf], (uint32_t)(((j - 2) >> 1) & 1), &abort_flag, 12)) {
+        if (!pf_wait_outlined(&bar_o[buf], (uint32_t)(((j - 2) >> 1) & 1), &abort_flag, 12)) {
           ok = false;
           break;
         }
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(352, 1)
         // PV(j-1) must be complete before O is rescaled.  PV(j-3), on the same
         // barrier, was waited for above one tile ago, so this wait is never more
         // than one phase behind, and tiles that need no rescale need not wait.
-        if (!pf_wait(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 7)) {
+        if (!pf_wait_outlined(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 7)) {
           ok = false;
           break;
         }
@@ -429,14 +429,14 @@ __global__ void __launch_bounds__(352, 1)
     }
     if (ok && n > 0) {
       // the last P.V (the earlier ones are done or finish before it)
-      ok = pf_wait(&bar_o[(n - 1) & 1], (uint32_t)(((n - 1) >> 1) & 1), &abort_flag, 8);
+      ok = pf_wait_outlined(&bar_o[(n - 1) & 1], (uint32_t)(((n - 1) >> 1) & 1), &abort_flag, 8);
       tc_fence_after_sync();
     }
     // the row's sums are split over the two halves
     xch_l[half][row] = l_run;
     xch_lr[half][row] = lr_run;
     mbar_arrive(&bar_xe[wq]);
-    if (ok) ok = pf_wait(&bar_xe[wq], 0, &abort_flag, 10);
+    if (ok) ok = pf_wait_outlined(&bar_xe[wq], 0, &abort_flag, 10);
     l_run += xch_l[half ^ 1][row];
     lr_run += xch_lr[half ^ 1][row];
     if (ok) {

@@ -197,6 +197,14 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// Eight 32-bit words to global memory in one 256-bit store (32-byte aligned address).
+__device__ __forceinline__ void st_global_v8(void* ptr, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                             uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w0), "r"(w1), "r"(w2),
+               "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive 32-bit columns written to this thread's TMEM lane.

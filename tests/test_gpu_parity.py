@@ -271,6 +271,65 @@ def test_jagged_parity_and_worklist(causal, D):
         assert all(r[0] == seq[0][0] for r in seq) and u[1] == (seq[0][1] + block_m - 1) // block_m
 
 
+@pytest.mark.parametrize("odd_high", [True, False])
+def test_jagged_extreme_score_jumps(odd_high):
+    """Keys in every other 128-key tile of a sequence score ~196 log2 units above the
+    rest, so between consecutive KV tiles the running max jumps (or the tile adds only
+    weights that underflow to zero in fp32): the online-softmax rescale factor is 0 and
+    the lazily raised reference must still give the exact mean of the high keys' V.
+    The lengths include lone last Q tiles and partial tiles of both parities."""
+    lengths = [300, 640, 1100, 385, 1000]
+    H, D = 2, 128
+    offs = syn.offsets_from_lengths(lengths)
+    T = int(offs[-1])
+    q, k, v = syn.qkv((T, H, D), (T, H, D), "bf16", 31, "cuda")
+    pos = torch.arange(T, device="cuda")
+    rel = pos - torch.from_numpy(offs[:-1].astype(np.int64)).cuda().repeat_interleave(
+        torch.tensor(lengths, device="cuda"))
+    odd = ((rel // 128) % 2 == 1)[:, None, None]
+    hi = odd if odd_high else ~odd
+    q = (2.0 + 0.1 * q.float()).to(torch.bfloat16)
+    k = torch.where(hi, 3.0 + 0.1 * k.float(), -3.0 + 0.1 * k.float()).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(H, T, device="cuda")
+    ws = torch.empty(ra.attn_jagged_workspace_bytes(len(lengths), T, max(lengths)), dtype=torch.uint8,
+                     device="cuda")
+    ra.attn_jagged(q, k, v, o, torch.from_numpy(offs).cuda(), max(lengths), ws, lse, causal=True)
+    O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), True)
+    close_o(o, O)
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_output_base_16_bytes_past_32(D):
+    """The paired kernel stores O rows in 32-byte pieces when the output's base allows
+    it and in 16-byte pieces otherwise: outputs 16 bytes past a 32-byte boundary."""
+    B, S_, h = 1, 300, 2
+    q, k, v = gen((B, S_, h, D), (B, S_, h, D), "bf16", seed=77)
+    buf = torch.zeros(q.numel() + 16, dtype=q.dtype, device="cuda")
+    o = buf[8:8 + q.numel()].view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty(B, h, S_, device="cuda")
+    ra.attn_prefill(q, k, v, o, lse, causal=True)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), True)
+    close_o(o, O, "dense, offset output")
+    close_lse(lse, L)
+    assert torch.all(buf[:8] == 0) and torch.all(buf[8 + q.numel():] == 0)
+    lengths = [300, 77, 640]
+    offs = syn.offsets_from_lengths(lengths)
+    T = int(offs[-1])
+    q, k, v = syn.qkv((T, h, D), (T, h, D), "bf16", 78, "cuda")
+    buf = torch.zeros(q.numel() + 16, dtype=q.dtype, device="cuda")
+    o = buf[8:8 + q.numel()].view(q.shape)
+    lse = torch.empty(h, T, device="cuda")
+    ws = torch.empty(ra.attn_jagged_workspace_bytes(len(lengths), T, 640), dtype=torch.uint8, device="cuda")
+    ra.attn_jagged(q, k, v, o, torch.from_numpy(offs).cuda(), 640, ws, lse, causal=True)
+    O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), True)
+    close_o(o, O, "jagged, offset output")
+    close_lse(lse, L)
+    assert torch.all(buf[:8] == 0) and torch.all(buf[8 + q.numel():] == 0)
+
+
 def test_jagged_random_lengths():
     rng = np.random.default_rng(3)
     lengths = rng.integers(0, 700, 40)
