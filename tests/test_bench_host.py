@@ -62,3 +62,21 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_nonzero_rank_is_silent():
     r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "1"], {"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_roofline_objects():
+    """Achieved = algorithmic units per launch / launch time; a workload bound by HBM
+    (below the ridge point) reports its tensor fraction beside the binding roofline."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    dense = {"bound": "tensor", "kernel_units": 0.55}  # TFLOP per launch
+    r = bench.roofline(dense, 0.5, peaks, "measured", traffic=123)
+    assert r == {"bound": "tensor", "achieved": 1100.0, "peak": 2000.0, "unit": "TFLOP/s", "frac": 0.55,
+                 "traffic": 123, "peak_source": "measured"}
+    assert bench.tensor_roofline(dense, 0.5, peaks, "measured") == {}
+    jag = {"bound": "hbm", "kernel_units": 2.4, "tensor_units": 0.45}  # GB and TFLOP per launch
+    r = bench.roofline(jag, 0.8, peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["achieved"] == 3000.0 and r["frac"] == 0.5
+    t = bench.tensor_roofline(jag, 0.8, peaks, "measured")["roofline_tensor"]
+    assert t["achieved"] == 562.5 and t["frac"] == 0.2812 and t["unit"] == "TFLOP/s"
