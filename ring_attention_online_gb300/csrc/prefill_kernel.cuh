@@ -63,7 +63,9 @@ struct PrefillCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool kBf16, int kMode>
+// kOneChunk: the launch walks a single chunk (no ring order); the literal lets
+// the compiler drop the ring-order walk state
+template <int D, bool kBf16, int kMode, bool kOneChunk>
 __global__ void __launch_bounds__(352, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
@@ -109,7 +111,8 @@ __global__ void __launch_bounds__(352, 1)
   }
   const int hk = h / p.group;
   TileWalk walk;
-  walk.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, p.num_chunks, C::BN, kMode == kModeWindow ? p.window : -1);
+  walk.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, kOneChunk ? 1 : p.num_chunks, C::BN,
+            kMode == kModeWindow ? p.window : -1);
   const int n = walk.count();
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -510,36 +513,43 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D, bool kBf16, int kMode>
+template <int D, bool kBf16, int kMode, bool kOneChunk>
 attn_status_t launch_prefill_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                      const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
   using C = PrefillCfg<D>;
-  auto kern = prefill_kernel<D, kBf16, kMode>;
+  auto kern = prefill_kernel<D, kBf16, kMode, kOneChunk>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Dense and window launches with one chunk, and every partial and jagged
+// launch (always one KV range), take the single-chunk instantiations.
+template <int D, bool kBf16>
+attn_status_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                   const CUtensorMap& mv, int mode, dim3 grid, cudaStream_t s) {
+  const bool one = p.num_chunks == 1;
+  switch (mode) {
+    case kModeDense:
+      return one ? launch_prefill_variant<D, kBf16, kModeDense, true>(p, mq, mk, mv, grid, s)
+                 : launch_prefill_variant<D, kBf16, kModeDense, false>(p, mq, mk, mv, grid, s);
+    case kModeWindow:
+      return one ? launch_prefill_variant<D, kBf16, kModeWindow, true>(p, mq, mk, mv, grid, s)
+                 : launch_prefill_variant<D, kBf16, kModeWindow, false>(p, mq, mk, mv, grid, s);
+    case kModePartial:
+      return one ? launch_prefill_variant<D, kBf16, kModePartial, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+    case kModeJagged:
+      return one ? launch_prefill_variant<D, kBf16, kModeJagged, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_ERR_INVALID_ARG;
+}
+
 template <int D>
 attn_status_t launch_prefill_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                       const CUtensorMap& mv, int mode, bool bf16, dim3 grid, cudaStream_t s) {
-  if (bf16) {
-    switch (mode) {
-      case kModeDense: return launch_prefill_variant<D, true, kModeDense>(p, mq, mk, mv, grid, s);
-      case kModePartial: return launch_prefill_variant<D, true, kModePartial>(p, mq, mk, mv, grid, s);
-      case kModeJagged: return launch_prefill_variant<D, true, kModeJagged>(p, mq, mk, mv, grid, s);
-      case kModeWindow: return launch_prefill_variant<D, true, kModeWindow>(p, mq, mk, mv, grid, s);
-    }
-  } else {
-    switch (mode) {
-      case kModeDense: return launch_prefill_variant<D, false, kModeDense>(p, mq, mk, mv, grid, s);
-      case kModePartial: return launch_prefill_variant<D, false, kModePartial>(p, mq, mk, mv, grid, s);
-      case kModeJagged: return launch_prefill_variant<D, false, kModeJagged>(p, mq, mk, mv, grid, s);
-      case kModeWindow: return launch_prefill_variant<D, false, kModeWindow>(p, mq, mk, mv, grid, s);
-    }
-  }
-  return ATTN_ERR_INVALID_ARG;
+  return bf16 ? launch_prefill_typed<D, true>(p, mq, mk, mv, mode, grid, s)
+              : launch_prefill_typed<D, false>(p, mq, mk, mv, mode, grid, s);
 }
 
 }  // namespace attn

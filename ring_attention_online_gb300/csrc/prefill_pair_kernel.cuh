@@ -153,7 +153,11 @@ __device__ __forceinline__ int pair_item_index(int r, int total) {
   return k < total ? (int)k : -2;  // -2: none this round, and none later
 }
 
-template <int D, bool kBf16, int kMode>
+// kOneChunk: the launch walks a single chunk (no ring order); the literal lets
+// the compiler drop the ring-order walk state from every loop, which matters
+// at this kernel's register limit (jagged 472 -> 558 TFLOP/s, sliding window
+// 943 -> 1040)
+template <int D, bool kBf16, int kMode, bool kOneChunk>
 // 11 warps put three on three of the four SM sub-partitions (16K registers
 // each), so at most 168 registers per thread
 __global__ void __launch_bounds__(352, 1)
@@ -208,11 +212,8 @@ __global__ void __launch_bounds__(352, 1)
   auto item_walk = [&](const PairItem& it, TileWalk& walk) -> int {
     const int u_lo = it.st0.q_lo;
     const int u_hi = it.st1.empty() ? it.st0.q_hi : max(it.st0.q_hi, it.st1.q_hi);
-    // (jagged walks have a single chunk: the literal lets the compiler drop
-    // the ring-order state from the loops, which took the jagged kernel off
-    // its register limit and made it 18 % faster)
-    walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal,
-              kMode == kModeJagged ? 1 : p.num_chunks, C::BN, kMode == kModeWindow ? p.window : -1);
+    walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, kOneChunk ? 1 : p.num_chunks, C::BN,
+              kMode == kModeWindow ? p.window : -1);
     return walk.count();
   };
   auto active = [&](const PairItem& it, int x, int ks) -> bool {
@@ -640,36 +641,43 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D, bool kBf16, int kMode>
+template <int D, bool kBf16, int kMode, bool kOneChunk>
 attn_status_t launch_pair_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
   using C = PairCfg<D>;
-  auto kern = prefill_pair_kernel<D, kBf16, kMode>;
+  auto kern = prefill_pair_kernel<D, kBf16, kMode, kOneChunk>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Dense and window launches with one chunk, and every partial and jagged
+// launch (always one KV range), take the single-chunk instantiations.
+template <int D, bool kBf16>
+attn_status_t launch_pair_typed(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                const CUtensorMap& mv, int mode, dim3 grid, cudaStream_t s) {
+  const bool one = p.num_chunks == 1;
+  switch (mode) {
+    case kModeDense:
+      return one ? launch_pair_variant<D, kBf16, kModeDense, true>(p, mq, mk, mv, grid, s)
+                 : launch_pair_variant<D, kBf16, kModeDense, false>(p, mq, mk, mv, grid, s);
+    case kModeWindow:
+      return one ? launch_pair_variant<D, kBf16, kModeWindow, true>(p, mq, mk, mv, grid, s)
+                 : launch_pair_variant<D, kBf16, kModeWindow, false>(p, mq, mk, mv, grid, s);
+    case kModePartial:
+      return one ? launch_pair_variant<D, kBf16, kModePartial, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+    case kModeJagged:
+      return one ? launch_pair_variant<D, kBf16, kModeJagged, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_ERR_INVALID_ARG;
+}
+
 template <int D>
 attn_status_t launch_pair_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                    const CUtensorMap& mv, int mode, bool bf16, dim3 grid, cudaStream_t s) {
-  if (bf16) {
-    switch (mode) {
-      case kModeDense: return launch_pair_variant<D, true, kModeDense>(p, mq, mk, mv, grid, s);
-      case kModePartial: return launch_pair_variant<D, true, kModePartial>(p, mq, mk, mv, grid, s);
-      case kModeJagged: return launch_pair_variant<D, true, kModeJagged>(p, mq, mk, mv, grid, s);
-      case kModeWindow: return launch_pair_variant<D, true, kModeWindow>(p, mq, mk, mv, grid, s);
-    }
-  } else {
-    switch (mode) {
-      case kModeDense: return launch_pair_variant<D, false, kModeDense>(p, mq, mk, mv, grid, s);
-      case kModePartial: return launch_pair_variant<D, false, kModePartial>(p, mq, mk, mv, grid, s);
-      case kModeJagged: return launch_pair_variant<D, false, kModeJagged>(p, mq, mk, mv, grid, s);
-      case kModeWindow: return launch_pair_variant<D, false, kModeWindow>(p, mq, mk, mv, grid, s);
-    }
-  }
-  return ATTN_ERR_INVALID_ARG;
+  return bf16 ? launch_pair_typed<D, true>(p, mq, mk, mv, mode, grid, s)
+              : launch_pair_typed<D, false>(p, mq, mk, mv, mode, grid, s);
 }
 
 }  // namespace attn
