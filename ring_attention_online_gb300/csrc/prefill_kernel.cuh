@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t pcol = lane_addr + C::P_COL + static_cast<uint32_t>(buf * 64);
       const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
       const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
-      uint64_t sum2 = f2_make(0.f, 0.f), sumr2 = f2_make(0.f, 0.f);
+      uint64_t sum2 = f2_make(0.f, 0.f);
+      float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // rounded weights, 8 chains
       uint32_t pk[16];
       auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
 #pragma unroll
@@ -394,17 +395,16 @@ __global__ void __launch_bounds__(352, 1)
           sum2 = f2_add(sum2, f2_make(p0, p1));
           // O is normalised by the sum of the rounded weights it was built
           // from, so O / l is a weighted mean with consistent weights
-          const float2 pr = unpack_half2<kBf16>(pk[i]);
-          sumr2 = f2_add(sumr2, f2_make(pr.x, pr.y));
+          add_half2_to_f32<kBf16>(sr[2 * (i & 3)], sr[2 * (i & 3) + 1], pk[i]);
         }
         tmem_st16(pcol + col, pk);
       };
       // P(j) for keys [64*half, 64*half+64) goes to its columns [32*half, 32*half+32)
       pack_chunk(r0, half * 32);
       pack_chunk(r1, half * 32 + 16);
-      const float2 sv = f2_split(sum2), srv = f2_split(sumr2);
+      const float2 sv = f2_split(sum2);
       l_run += sv.x + sv.y;
-      lr_run += srv.x + srv.y;
+      lr_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
 
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
         // PV(j-1) must be complete before O is rescaled.  PV(j-3), on the same

@@ -317,6 +317,23 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// a += the low 16-bit float of w, b += the high one, each converted exactly
+// and added in fp32: one mixed-precision add per value, where unpacking to
+// fp32 first costs a shift or mask per value plus the add.
+template <bool kBf16>
+__device__ __forceinline__ void add_half2_to_f32(float& a, float& b, uint32_t w) {
+  if constexpr (kBf16)
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(w));
+  else
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.f16 %0, lo, %0;\n\t"
+        "add.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(w));
+}
+
 // Inverse of pack_half2: the two 16-bit floats of w as fp32 (exact).
 template <bool kBf16>
 __device__ __forceinline__ float2 unpack_half2(uint32_t w) {
