@@ -198,12 +198,47 @@ def make_workload(name: str, device, batch=None, seq=None):
                               "h_kv": cfg["h_kv"], "D": cfg["D"], "causal": causal, "num_chunks": C,
                               "tile": "128x128", "l2": "inputs larger than L2 (no flush)"},
                              **({"window": window} if window is not None else {})))
+        pipe = {}
+
         def e2e_step(host_in, host_out, stream):
-            for d, h in zip((q, k, v), host_in):
-                d.copy_(h, non_blocking=True)
-            step(stream)
-            for h, d in zip(host_out, (o, lse)):
-                h.copy_(d, non_blocking=True)
+            """One batch at a time through the public entry point, with the batches
+            pipelined over three streams: batch b+1's inputs copy in while batch b
+            computes and batch b-1's outputs copy out (the link runs both ways at
+            once).  Events keep each batch's buffers from being overwritten before
+            the previous step has used them."""
+            B = cfg["B"]
+            if not pipe:
+                pipe.update(h2d=torch.cuda.Stream(device), d2h=torch.cuda.Stream(device), started=False,
+                            ev_in=[torch.cuda.Event() for _ in range(B)],
+                            ev_c=[torch.cuda.Event() for _ in range(B)],
+                            ev_out=[torch.cuda.Event() for _ in range(B)])
+            h2d, d2h = pipe["h2d"], pipe["d2h"]
+            pipe.setdefault("ev_start", torch.cuda.Event()).record(stream)
+            h2d.wait_event(pipe["ev_start"])  # the copies start inside the step
+            for b in range(B):
+                if pipe["started"]:
+                    h2d.wait_event(pipe["ev_c"][b])  # the previous step has read batch b's inputs
+                with torch.cuda.stream(h2d):
+                    for d, h in zip((q, k, v), host_in):
+                        d[b].copy_(h[b], non_blocking=True)
+                pipe["ev_in"][b].record(h2d)
+                stream.wait_event(pipe["ev_in"][b])
+                if pipe["started"]:
+                    stream.wait_event(pipe["ev_out"][b])  # ... and copied out batch b's outputs
+                sl = slice(b, b + 1)
+                if window is None:
+                    ra.attn_prefill(q[sl], k[sl], v[sl], o[sl], lse[sl], causal=causal, num_chunks=C, stream=stream)
+                else:
+                    ra.attn_prefill_window(q[sl], k[sl], v[sl], o[sl], lse[sl], window=window, num_chunks=C,
+                                           stream=stream)
+                pipe["ev_c"][b].record(stream)
+                d2h.wait_event(pipe["ev_c"][b])
+                with torch.cuda.stream(d2h):
+                    for h, d in zip(host_out, (o, lse)):
+                        h[b].copy_(d[b], non_blocking=True)
+                pipe["ev_out"][b].record(d2h)
+            pipe["started"] = True
+            stream.wait_event(pipe["ev_out"][B - 1])  # the step ends with its last output on the host
         w["e2e_step"] = e2e_step
     elif cfg["kind"] == "jagged":
         q, k, v, offs = syn.jagged_inputs(cfg, seed=0, device=device)
