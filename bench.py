@@ -92,6 +92,22 @@ def aggregate(per_rank_units: float, per_rank_ms: float, world: int, device=None
     return per_rank_units * world, ms
 
 
+# Nominal denominators, beside the measured ones: dense bf16 tcgen05 rate per SM
+# (a 128x128x16 kind::f16 MMA issues every 64 cycles back to back on one SM, as a
+# microbenchmark on this GPU confirmed) x SMs x the maximum SM clock, and the
+# published HBM3e bandwidth.
+BF16_FLOP_PER_CLK_PER_SM = 128 * 128 * 16 * 2 // 64
+NOMINAL_HBM_GBS = 7900.0
+
+
+def nominal_peaks(device, peaks):
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    return {"tflops": sms * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12, "hbm_gbs": NOMINAL_HBM_GBS,
+            "basis": f"{sms} SMs x {mhz:.0f} MHz x {BF16_FLOP_PER_CLK_PER_SM} bf16 FLOP/clk/SM; HBM3e 7.9 TB/s"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -302,27 +318,30 @@ def time_steps(step, K: int, W: int, device):
     return start.elapsed_time(end)
 
 
-def roofline(w, kernel_ms_per_launch: float, peaks, peak_kind: str, traffic=None):
+def roofline(w, kernel_ms_per_launch: float, peaks, peak_kind: str, traffic=None, nominal=None):
+    achieved = w["kernel_units"] / (kernel_ms_per_launch / 1e3)
     if w["bound"] == "tensor":
-        achieved = w["kernel_units"] / (kernel_ms_per_launch / 1e3)
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
+        peak, unit, nom = peaks["bf16_tflops"], "TFLOP/s", (nominal or {}).get("tflops")
     else:
-        achieved = w["kernel_units"] / (kernel_ms_per_launch / 1e3)
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    return {"bound": w["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_kind}
+        peak, unit, nom = peaks["hbm_gbs"], "GB/s", (nominal or {}).get("hbm_gbs")
+    r = {"bound": w["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_kind}
+    if nom:
+        r["nominal"] = {"peak": round(nom, 1), "frac": round(achieved / nom, 4), "basis": nominal["basis"]}
+    return r
 
 
-def tensor_roofline(w, kernel_ms_per_launch: float, peaks, peak_kind: str):
+def tensor_roofline(w, kernel_ms_per_launch: float, peaks, peak_kind: str, nominal=None):
     """The tensor-core fraction of a workload whose binding roofline is HBM."""
     if "tensor_units" not in w:
         return {}
     tfs = w["tensor_units"] / (kernel_ms_per_launch / 1e3)
-    return {"roofline_tensor": {"bound": "tensor", "achieved": round(tfs, 2), "peak": peaks["bf16_tflops"],
-                                "unit": "TFLOP/s", "frac": round(tfs / peaks["bf16_tflops"], 4),
-                                "peak_source": peak_kind}}
+    r = {"bound": "tensor", "achieved": round(tfs, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+         "frac": round(tfs / peaks["bf16_tflops"], 4), "peak_source": peak_kind}
+    if nominal:
+        r["nominal"] = {"peak": round(nominal["tflops"], 1), "frac": round(tfs / nominal["tflops"], 4),
+                        "basis": nominal["basis"]}
+    return {"roofline_tensor": r}
 
 
 # ------------------------------------------------------------------ CPU legs (oracle)
@@ -401,6 +420,7 @@ def run_ours(args):
     import ring_attention_online_gb300 as ra
     ra.load_library()
     peaks, peak_kind = load_peaks()
+    nominal = nominal_peaks(device, peaks)
     K, W = args.steps, max(args.warmup, 3)
 
     # ---- headline (or the workload named on the command line)
@@ -426,8 +446,8 @@ def run_ours(args):
             "vs_baseline": round(value / world / PAGES_DENSE_CAUSAL_TFS, 3) if args.workload == HEADLINE and
             args.batch is None and args.seq is None else None, "dtype": "bf16", "data": "synthetic",
             "config": dict(w["config"], parallelism=f"replicas{world}" if world > 1 else "single"),
-            "roofline": roofline(w, kernel_ms, peaks, peak_kind, traffic),
-            **tensor_roofline(w, kernel_ms, peaks, peak_kind),
+            "roofline": roofline(w, kernel_ms, peaks, peak_kind, traffic, nominal),
+            **tensor_roofline(w, kernel_ms, peaks, peak_kind, nominal),
             "gpu_launches": K * w["launches"],
             "clocks": clk}
 
@@ -460,8 +480,8 @@ def run_ours(args):
             kernel_ms = ms2 / k2
             entry = {"workload": name, "value": round(units2 / (ms2_max / 1e3), 2), "unit": w["unit"],
                      "ms_per_step": round(ms2_max / k2, 4), "steps": k2, "config": w["config"],
-                     "roofline": roofline(w, kernel_ms, peaks, peak_kind, _profiled_traffic(name))}
-            entry.update(tensor_roofline(w, kernel_ms, peaks, peak_kind))
+                     "roofline": roofline(w, kernel_ms, peaks, peak_kind, _profiled_traffic(name), nominal)}
+            entry.update(tensor_roofline(w, kernel_ms, peaks, peak_kind, nominal))
             sec.append(entry)
             line["gpu_launches"] += k2 * w["launches"]
             status = ra.attn_last_device_status()

@@ -80,3 +80,10 @@ def test_roofline_objects():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["achieved"] == 3000.0 and r["frac"] == 0.5
     t = bench.tensor_roofline(jag, 0.8, peaks, "measured")["roofline_tensor"]
     assert t["achieved"] == 562.5 and t["frac"] == 0.2812 and t["unit"] == "TFLOP/s"
+    # nominal denominators beside the measured ones
+    nom = {"tflops": 2500.0, "hbm_gbs": 8000.0, "basis": "test"}
+    assert bench.roofline(dense, 0.5, peaks, "measured", nominal=nom)["nominal"] == {"peak": 2500.0, "frac": 0.44,
+                                                                                     "basis": "test"}
+    assert bench.roofline(jag, 0.8, peaks, "measured", nominal=nom)["nominal"]["frac"] == 0.375
+    assert bench.tensor_roofline(jag, 0.8, peaks, "measured", nom)["roofline_tensor"]["nominal"]["frac"] == 0.225
+    assert bench.BF16_FLOP_PER_CLK_PER_SM == 8192
