@@ -74,7 +74,9 @@ dim3 persistent_grid(long long items) {
 // batch).  False when the item count does not fit a 32-bit item index.
 bool dense_grid(PrefillParams& p, int D, dim3* grid) {
   if (!paired(D)) {
-    *grid = dim3((p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M, p.h_q, p.B);
+    // two Q tiles per CTA (see prefill_kernel.cuh)
+    const int n_qt = (p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M;
+    *grid = dim3((n_qt + 1) / 2, p.h_q, p.B);
     return true;
   }
   const int rows = p.pair_heads ? ATTN_BLOCK_M : 2 * ATTN_BLOCK_M;

@@ -1,5 +1,5 @@
-// Blockwise online-softmax attention forward, tcgen05 + TMA, one Q tile of
-// 128 rows per CTA.
+// Blockwise online-softmax attention forward, tcgen05 + TMA, Q tiles of 128
+// rows, two per CTA for dense launches.
 //
 // What it computes, by source:
 //  * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel: per KV block,
@@ -12,9 +12,20 @@
 //    at min(kv_end, tile_q.end) (no fully masked tile is visited); only the
 //    diagonal and tail tiles are masked.
 //
+// Work: a dense, partial or window CTA takes two Q tiles of one (batch,
+// head), t and n_qt - 1 - t when causal (so every CTA walks n_qt + 1 KV
+// tiles) or 2x and 2x + 1 otherwise, the longer first; a jagged CTA takes one
+// worklist item.  Barrier phases and the K/V stage ring run on from the first
+// item to the second, so the second item's Q and first K/V tiles load, and its
+// first S is computed, while the first item's last tiles and epilogue finish:
+// a CTA's fixed costs (start-up, first loads, pipeline fill) were ~11 K cycles
+// per Q tile, 18 % of the dense causal S=4096 launch.
+//
 // CTA layout (352 threads):
-//   warp 0      TMA producer: Q tile once, then K/V 128-column slabs through a
-//               ring of NST shared-memory stages: K(0), then per tile K(j+1), V(j).
+//   warp 0      TMA producer: per item the Q tile (once the previous item's S
+//               MMAs are done with the Q buffer), then K/V 128-column slabs
+//               through a ring of NST shared-memory stages: K(0), then per
+//               tile K(j+1), V(j).
 //   warp 1      TMEM owner and S issuer: S(j) = Q.K_j^T into one of two
 //               128-column TMEM buffers, once PV(j-2) has read that buffer.
 //   warp 10     PV issuer: O += P(j).V_j, P(j) (bf16/fp16, written over S(j) by
@@ -71,7 +82,7 @@ __global__ void __launch_bounds__(352, 1)
                    const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = PrefillCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_fin;
+  __shared__ uint64_t bar_q, bar_qe, bar_fin;  // Q landed; Q buffer free (the item's S MMAs done)
   __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2]
   __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
   __shared__ uint64_t bar_s[2], bar_p[2];
@@ -79,41 +90,63 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
   __shared__ float xch_max[2][2][128];  // [tile parity][column half][row]
-  __shared__ float xch_l[2][128], xch_lr[2][128];
+  __shared__ float xch_l[2][2][128], xch_lr[2][2][128];  // [item parity][column half][row]
   __shared__ uint64_t bar_x[2][4];       // pair exchange barriers: [tile parity][lane quarter]
   __shared__ uint64_t bar_xe[4];         // end-of-row exchange barrier per lane quarter
 
-  // ------------------------------------------------------------ work item
-  int b, h, q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0;
+  // ------------------------------------------------------------ work items
+  struct Item {
+    int b, h, q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0;
+  };
+  int n_my = 1;  // items of this CTA
+  int t_first = 0, t_second = 0;
   if constexpr (kMode == kModeJagged) {
-    const int item = blockIdx.x;
-    if (item >= *p.work_count) return;  // the grid is an upper bound on the item count
-    const int4 it = p.work_items[item];
-    b = 0;
-    h = blockIdx.y;
-    q_lo = it.z;
-    q_hi = it.z + it.w;
-    kv_lo = it.x;
-    kv_hi = it.x + it.y;  // seq_offsets[seq_idx + 1]
-    q_pos0 = 0;
-    kv_pos0 = 0;
+    if ((int)blockIdx.x >= *p.work_count) return;  // the grid is an upper bound on the item count
   } else {
-    // causal: longest Q tiles first, so the short ones fill the tail
-    const int qt = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-    b = blockIdx.z;
-    h = blockIdx.y;
-    q_lo = qt * C::BM;
-    q_hi = min(q_lo + C::BM, p.S_q);
-    kv_lo = p.kv_lo;
-    kv_hi = p.kv_hi;
-    q_pos0 = p.q_pos0;
-    kv_pos0 = p.kv_pos0;
+    const int n_qt = (p.S_q + C::BM - 1) / C::BM;
+    const int x = (int)blockIdx.x;
+    if (p.causal) {
+      t_first = n_qt - 1 - x;
+      t_second = x;
+      n_my = t_second < t_first ? 2 : 1;
+    } else {
+      t_first = 2 * x;
+      t_second = 2 * x + 1;
+      n_my = t_second < n_qt ? 2 : 1;
+    }
   }
-  const int hk = h / p.group;
-  TileWalk walk;
-  walk.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, p.causal, kOneChunk ? 1 : p.num_chunks, C::BN,
-            kMode == kModeWindow ? p.window : -1);
-  const int n = walk.count();
+  auto get_item = [&](int i) -> Item {
+    Item it;
+    if constexpr (kMode == kModeJagged) {
+      (void)i;
+      const int4 w = p.work_items[blockIdx.x];
+      it.b = 0;
+      it.h = blockIdx.y;
+      it.q_lo = w.z;
+      it.q_hi = w.z + w.w;
+      it.kv_lo = w.x;
+      it.kv_hi = w.x + w.y;  // seq_offsets[seq_idx + 1]
+      it.q_pos0 = 0;
+      it.kv_pos0 = 0;
+    } else {
+      const int qt = i == 0 ? t_first : t_second;
+      it.b = blockIdx.z;
+      it.h = blockIdx.y;
+      it.q_lo = qt * C::BM;
+      it.q_hi = min(it.q_lo + C::BM, p.S_q);
+      it.kv_lo = p.kv_lo;
+      it.kv_hi = p.kv_hi;
+      it.q_pos0 = p.q_pos0;
+      it.kv_pos0 = p.kv_pos0;
+    }
+    return it;
+  };
+  auto item_walk = [&](const Item& it, TileWalk& w) -> int {
+    w.init(it.q_lo, it.q_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, kOneChunk ? 1 : p.num_chunks, C::BN,
+           kMode == kModeWindow ? p.window : -1);
+    return w.count();
+  };
+  const int hk = (int)blockIdx.y / p.group;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -124,6 +157,7 @@ __global__ void __launch_bounds__(352, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_qe, 1);
     mbar_init(&bar_o[0], 1);
     mbar_init(&bar_o[1], 1);
     mbar_init(&bar_fin, 2);  // one commit per MMA issuer
@@ -151,23 +185,22 @@ __global__ void __launch_bounds__(352, 1)
 
   if (warp == 0) {
     // ========================================================== TMA producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
-      mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
-      for (int blk = 0; blk < D / 64; ++blk) tma_load_4d(sQ + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, h, q_lo, b);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
+      int q_loads = 0;
       bool ok = true;
-      auto push = [&](const CUtensorMap* map, int start) -> bool {
+      auto push = [&](const CUtensorMap* map, int start, int bb) -> bool {
         for (int hs = 0; hs < C::NH; ++hs) {
           if (!pf_wait_outlined(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
           uint8_t* dst = sKV + stage * C::SLAB_BYTES;
           mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
           for (int blk = 0; blk < C::BLK_PER_SLAB; ++blk)
-            tma_load_4d(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], hs * C::SC + blk * 64, hk, start, b);
+            tma_load_4d(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], hs * C::SC + blk * 64, hk, start, bb);
           ++issued;
           if (++stage == C::NST) {
             stage = 0;
@@ -176,22 +209,37 @@ __global__ void __launch_bounds__(352, 1)
         }
         return true;
       };
-      TileWalk kw = walk, vw = walk;
-      int ch, st, me;
-      kw.next(ch, st, me);
-      ok = push(&mk, st);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          kw.next(ch, st, me);
-          ok = push(&mk, st);
-          if (!ok) break;
+      for (int i = 0; ok && i < n_my; ++i) {
+        const Item it = get_item(i);
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        // the Q buffer is free once the previous item's S MMAs are done
+        if (q_loads > 0 && !pf_wait_outlined(&bar_qe, (uint32_t)((q_loads - 1) & 1), &abort_flag, 13)) {
+          ok = false;
+          break;
         }
-        vw.next(ch, st, me);
-        ok = push(&mv, st);
+        mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(sQ + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, it.h, it.q_lo, it.b);
+        ++q_loads;
+        TileWalk kw = walk, vw = walk;
+        int ch, st, me;
+        kw.next(ch, st, me);
+        ok = push(&mk, st, it.b);
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n) {
+            kw.next(ch, st, me);
+            ok = push(&mk, st, it.b);
+            if (!ok) break;
+          }
+          vw.next(ch, st, me);
+          ok = push(&mv, st, it.b);
+        }
       }
       if (abort_flag) {
         // copies may still be landing in shared memory: wait for them
-        pf_drain(&bar_q, 0);
+        if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
         const int outstanding = issued < C::NST ? issued : C::NST;
         for (int i = 0; i < outstanding; ++i) {
           const int pos = issued - 1 - i;
@@ -208,15 +256,16 @@ __global__ void __launch_bounds__(352, 1)
     // issuer on K stages and on PV(j-2) (S(j) overwrites P(j-2) in its TMEM
     // buffer, and MMAs of different threads are not ordered), the PV issuer on
     // P(j) and V stages.
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, C::SC, kBf16, true);
       const uint32_t skv = smem_u32(sKV);
-      // stage order of the producer: K(0), then per tile K(j+1), V(j); in
-      // tiles of NH slabs, K(j) is tile 2j - 1 (j > 0) and V(j) tile 2j + 2,
-      // except V(n - 1), the last tile, 2n - 1
-      auto k_tile = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
-      auto v_tile = [&](int j) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; };
+      // stage order of the producer within an item: K(0), then per tile
+      // K(j+1), V(j); in tiles of NH slabs, K(j) is tile 2j - 1 (j > 0) and
+      // V(j) tile 2j + 2, except V(n - 1), the last tile, 2n - 1; an item's
+      // 2n tiles follow the previous item's in the ring
+      auto k_tile = [](int j) { return j == 0 ? 0 : 2 * j - 1; };
+      auto v_tile = [](int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; };
       // each slab is waited for right before its MMAs, so the first half of S(j)
       // (PV(j)) can run while the second half's K (V) is still landing
       auto wait_slab = [&](int s, uint32_t site) -> bool {
@@ -225,57 +274,72 @@ __global__ void __launch_bounds__(352, 1)
         return true;
       };
       bool ok = true;
-      if (warp == 1) {
-        const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-        ok = pf_wait_outlined(&bar_q, 0, &abort_flag, 5);
-        tc_fence_after_sync();
-        for (int j = 0; ok && j < n; ++j) {
-          if (j >= 1) {
-            // the one S buffer is free once the softmax warps have read S(j-1)
-            ok = pf_wait_outlined(&bar_sfree[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 11);
-            if (!ok) break;
-            tc_fence_after_sync();
-          }
-          const int kt = k_tile(j);
-          const uint32_t d_tmem = tmem;
-          for (int hs = 0; hs < C::NH; ++hs) {
-            const int stage = (kt * C::NH + hs) % C::NST;
-            ok = wait_slab(kt * C::NH + hs, 2);
-            if (!ok) break;
-            const uint64_t kdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < C::SC / 16; ++ks) {
-              const uint32_t qoff = (hs * C::BLK_PER_SLAB + ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-              const uint32_t koff = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
-              mma_ss(d_tmem, desc_advance(qdesc, qoff), desc_advance(kdesc, koff), kIdescS, (hs | ks) != 0);
+      int g = 0;          // S (or PV) groups issued so far, all items: its barrier phases
+      int slab_base = 0;  // first slab of the current item
+      int q_used = 0;     // Q tiles consumed (S issuer)
+      for (int i = 0; ok && i < n_my; ++i) {
+        const Item it = get_item(i);
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        if (warp == 1) {
+          const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+          ok = pf_wait_outlined(&bar_q, (uint32_t)(q_used & 1), &abort_flag, 5);
+          tc_fence_after_sync();
+          ++q_used;
+          for (int j = 0; ok && j < n; ++j, ++g) {
+            if (g >= 1) {
+              // the one S buffer is free once the softmax warps have read the previous S
+              ok = pf_wait_outlined(&bar_sfree[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), &abort_flag, 11);
+              if (!ok) break;
+              tc_fence_after_sync();
             }
-            mma_commit(&bar_empty[stage]);
-          }
-          if (!ok) break;
-          mma_commit(&bar_s[j & 1]);
-        }
-      } else {
-        for (int j = 0; ok && j < n; ++j) {
-          ok = pf_wait_outlined(&bar_p[j & 1], (uint32_t)((j >> 1) & 1), &abort_flag, 3);
-          if (!ok) break;
-          const int vt = v_tile(j);
-          tc_fence_after_sync();  // P(j) in TMEM
-          const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((j & 1) * 64);
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
-          for (int hs = 0; hs < C::NH; ++hs) {
-            const int stage = (vt * C::NH + hs) % C::NST;
-            ok = wait_slab(vt * C::NH + hs, 4);
-            if (!ok) break;
-            const uint64_t vdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16384, 1024);
+            const int kt = k_tile(j);
+            const uint32_t d_tmem = tmem;
+            for (int hs = 0; hs < C::NH; ++hs) {
+              const int sl = slab_base + kt * C::NH + hs;
+              const int stage = sl % C::NST;
+              ok = wait_slab(sl, 2);
+              if (!ok) break;
+              const uint64_t kdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < C::BN / 16; ++ks)
-              mma_ts(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
-                     ks > 0 ? 1u : acc0);
-            mma_commit(&bar_empty[stage]);
+              for (int ks = 0; ks < C::SC / 16; ++ks) {
+                const uint32_t qoff = (hs * C::BLK_PER_SLAB + ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+                const uint32_t koff = (ks / 4) * C::BLOCK_BYTES + (ks % 4) * 32;
+                mma_ss(d_tmem, desc_advance(qdesc, qoff), desc_advance(kdesc, koff), kIdescS, (hs | ks) != 0);
+              }
+              mma_commit(&bar_empty[stage]);
+            }
+            if (!ok) break;
+            mma_commit(&bar_s[g & 1]);
           }
-          if (!ok) break;
-          mma_commit(&bar_o[j & 1]);
+          // the item's S MMAs, the last readers of its Q, release the Q buffer
+          if (ok) mma_commit(&bar_qe);
+        } else {
+          for (int j = 0; ok && j < n; ++j, ++g) {
+            ok = pf_wait_outlined(&bar_p[g & 1], (uint32_t)((g >> 1) & 1), &abort_flag, 3);
+            if (!ok) break;
+            const int vt = v_tile(j, n);
+            tc_fence_after_sync();  // P in TMEM
+            const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((g & 1) * 64);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;  // the item's first PV starts O afresh
+            for (int hs = 0; hs < C::NH; ++hs) {
+              const int sl = slab_base + vt * C::NH + hs;
+              const int stage = sl % C::NST;
+              ok = wait_slab(sl, 4);
+              if (!ok) break;
+              const uint64_t vdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16384, 1024);
+#pragma unroll
+              for (int ks = 0; ks < C::BN / 16; ++ks)
+                mma_ts(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                       ks > 0 ? 1u : acc0);
+              mma_commit(&bar_empty[stage]);
+            }
+            if (!ok) break;
+            mma_commit(&bar_o[g & 1]);
+          }
         }
+        slab_base += 2 * n * C::NH;
       }
       // every MMA either issuer issued must finish before TMEM is released
       mma_commit(&bar_fin);
@@ -291,21 +355,27 @@ __global__ void __launch_bounds__(352, 1)
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
     const int half = sw >> 2;
     const int row = wq * 32 + lane;
-    const int q_row = q_lo + row;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     constexpr int HD = D / 2;                                    // O columns per half
     const float c = p.scale_log2;  // > 0
+    bool ok = true;
+    int gj = 0;    // tiles so far, all items: the phases of the per-tile barriers
+    int n_ep = 0;  // epilogues so far
+    for (int i = 0; ok && i < n_my; ++i) {
+    const Item it = get_item(i);
+    TileWalk sw_walk;
+    const int n = item_walk(it, sw_walk);
+    const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
+    const int q_row = q_lo + row;
     float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
     float l_run = 0.f;             // this half's sum of exp2(x - m_run) in fp32: l and LSE
     float lr_run = 0.f;            // this half's sum of the rounded P the MMA multiplies V by
     float m_max = -CUDART_INF_F;   // true running max (partial mode)
-    bool ok = true;
-    TileWalk sw_walk = walk;
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < n; ++j, ++gj) {
       int ch, kstart, mend;
       sw_walk.next(ch, kstart, mend);
-      const int buf = j & 1;
-      if (!pf_wait_outlined(&bar_s[buf], (uint32_t)((j >> 1) & 1), &abort_flag, 6)) {
+      const int buf = gj & 1;
+      if (!pf_wait_outlined(&bar_s[buf], (uint32_t)((gj >> 1) & 1), &abort_flag, 6)) {
         ok = false;
         break;
       }
@@ -354,7 +424,7 @@ __global__ void __launch_bounds__(352, 1)
       // both halves of the row see each other's max
       xch_max[buf][half][row] = mx;
       mbar_arrive(&bar_x[buf][wq]);
-      if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((j >> 1) & 1), &abort_flag, 9)) {
+      if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((gj >> 1) & 1), &abort_flag, 9)) {
         ok = false;
         break;
       }
@@ -370,11 +440,11 @@ __global__ void __launch_bounds__(352, 1)
         l_run *= alpha;
         lr_run *= alpha;
       }
-      // P(j) goes to P buffer j % 2, which PV(j-2) read; PV(j-2) is waited for
-      // here and so always before PV(j) is issued (no waiter falls two phases
-      // behind on bar_o)
-      if (j >= 2) {
-        if (!pf_wait_outlined(&bar_o[buf], (uint32_t)(((j - 2) >> 1) & 1), &abort_flag, 12)) {
+      // P goes to P buffer gj % 2, which the PV two tiles back read; that PV is
+      // waited for here and so always before this tile's PV is issued (no
+      // waiter falls two phases behind on bar_o)
+      if (gj >= 2) {
+        if (!pf_wait_outlined(&bar_o[buf], (uint32_t)(((gj - 2) >> 1) & 1), &abort_flag, 12)) {
           ok = false;
           break;
         }
@@ -407,10 +477,11 @@ __global__ void __launch_bounds__(352, 1)
       lr_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
 
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        // PV(j-1) must be complete before O is rescaled.  PV(j-3), on the same
-        // barrier, was waited for above one tile ago, so this wait is never more
-        // than one phase behind, and tiles that need no rescale need not wait.
-        if (!pf_wait_outlined(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), &abort_flag, 7)) {
+        // the previous PV must be complete before O is rescaled.  The PV before
+        // it, on the same barrier, was waited for above one tile ago, so this
+        // wait is never more than one phase behind, and tiles that need no
+        // rescale need not wait.
+        if (!pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 7)) {
           ok = false;
           break;
         }
@@ -431,17 +502,20 @@ __global__ void __launch_bounds__(352, 1)
       mbar_arrive(&bar_p[buf]);
     }
     if (ok && n > 0) {
-      // the last P.V (the earlier ones are done or finish before it)
-      ok = pf_wait_outlined(&bar_o[(n - 1) & 1], (uint32_t)(((n - 1) >> 1) & 1), &abort_flag, 8);
+      // the item's last P.V (the earlier ones are done or finish before it)
+      ok = pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8);
       tc_fence_after_sync();
     }
-    // the row's sums are split over the two halves
-    xch_l[half][row] = l_run;
-    xch_lr[half][row] = lr_run;
+    // the row's sums are split over the two halves (one exchange buffer per
+    // item parity: a half cannot get two epilogues ahead of its partner)
+    const int ep = n_ep & 1;
+    xch_l[ep][half][row] = l_run;
+    xch_lr[ep][half][row] = lr_run;
     mbar_arrive(&bar_xe[wq]);
-    if (ok) ok = pf_wait_outlined(&bar_xe[wq], 0, &abort_flag, 10);
-    l_run += xch_l[half ^ 1][row];
-    lr_run += xch_lr[half ^ 1][row];
+    if (ok) ok = pf_wait_outlined(&bar_xe[wq], (uint32_t)ep, &abort_flag, 10);
+    ++n_ep;
+    l_run += xch_l[ep][half ^ 1][row];
+    lr_run += xch_lr[ep][half ^ 1][row];
     if (ok) {
       const bool row_valid = q_row < q_hi;
       const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
@@ -502,6 +576,7 @@ __global__ void __launch_bounds__(352, 1)
         }
       }
     }
+    }  // items
   }
 
   // ------------------------------------------------------------ teardown
