@@ -524,6 +524,7 @@ __global__ void __launch_bounds__(352, 1)
       if constexpr (kMode != kModePartial) {
         const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
         uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + half * HD;
+        const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll 1
         for (int cc = 0; cc < HD / 32; ++cc) {
           uint32_t o[32];
@@ -539,9 +540,17 @@ __global__ void __launch_bounds__(352, 1)
           for (int i = 0; i < 16; ++i)
             w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
           if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+            // a warp's store touches 32 rows: 32-byte pieces halve the requests
+            // of 16-byte ones (the output's base decides)
+            if (o_v8) {
+              st_global_v8(orow + cc * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              st_global_v8(orow + cc * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+            }
           }
         }
         if (p.lse != nullptr && row_valid && half == 0)
