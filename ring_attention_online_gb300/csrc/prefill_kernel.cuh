@@ -26,10 +26,11 @@
 //               MMAs are done with the Q buffer), then K/V 128-column slabs
 //               through a ring of NST shared-memory stages: K(0), then per
 //               tile K(j+1), V(j).
-//   warp 1      TMEM owner and S issuer: S(j) = Q.K_j^T into one of two
-//               128-column TMEM buffers, once PV(j-2) has read that buffer.
-//   warp 10     PV issuer: O += P(j).V_j, P(j) (bf16/fp16, written over S(j) by
-//               the softmax warps) being the TMEM A operand.
+//   warp 1      TMEM owner and S issuer: S(j) = Q.K_j^T into the one
+//               128-column S buffer, once the softmax warps have read S(j-1)
+//               out of it.
+//   warp 10     PV issuer: O += P(j).V_j, P(j) (bf16/fp16, written by the
+//               softmax warps to P buffer j mod 2) being the TMEM A operand.
 //   warps 2..9  softmax + epilogue: each query row (TMEM lane) is shared by two
 //               warps, one per half of the tile's 128 keys and of O's columns.
 //               Scores are scaled into the exp2 domain; the running max is
@@ -37,9 +38,9 @@
 //               rescaled in TMEM only on those tiles - the result is the same
 //               up to rounding because l and O always share one reference max.
 //
-// Every wait is bounded (see mbar_wait_bounded); a timeout sets the library's
-// device status, the CTA skips its remaining work, drains its copies and MMAs
-// and frees TMEM before returning.
+// Every wait is bounded (see pf_wait); a timeout sets the library's device
+// status, the CTA skips its remaining work, drains its copies and MMAs and
+// frees TMEM before returning.
 #pragma once
 
 #include <math_constants.h>
