@@ -127,18 +127,23 @@ def test_prefill_unequal_lengths(S_q, S_kv, causal):
     close_lse(lse, L)
 
 
-def test_prefill_empty_kv_gives_zero_and_neg_inf():
-    q, k, v = gen((1, 130, 2, 64), (1, 0, 2, 64), "bf16", seed=3)
-    k = torch.empty(1, 1, 2, 64, device="cuda", dtype=torch.bfloat16)  # any valid pointer
+@pytest.mark.parametrize("D,S_q", [(64, 130), (128, 300), (256, 300), (256, 130)])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_prefill_empty_kv_gives_zero_and_neg_inf(D, S_q, causal):
+    """No keys: O = 0 and LSE = -inf for every row.  At head dim 256 a CTA takes two Q
+    tiles in turn (S_q = 300: three tiles, one CTA with two empty items)."""
+    q, _, _ = gen((1, S_q, 2, D), (1, 1, 2, D), "bf16", seed=3)
+    k = torch.empty(1, 1, 2, D, device="cuda", dtype=torch.bfloat16)  # any valid pointer
     o = torch.full_like(q, 7.0)
-    lse = torch.zeros(1, 2, 130, device="cuda")
+    lse = torch.zeros(1, 2, S_q, device="cuda")
     lib = ra.load_library()
     import ctypes
     st = lib.attn_prefill(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(k.data_ptr()),
-                          ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(lse.data_ptr()), 1, 130, 0, 2, 2, 64, 1,
-                          0.125, 1, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                          ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(lse.data_ptr()), 1, S_q, 0, 2, 2, D, 1,
+                          1 / math.sqrt(D), causal, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0
     torch.cuda.synchronize()
+    assert ra.attn_last_device_status() == 0
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
 
 
