@@ -101,11 +101,20 @@ NOMINAL_HBM_GBS = 7900.0
 
 
 def nominal_peaks(device, peaks):
+    """SMs x maximum SM clock x the per-SM bf16 rate, which the library's probe
+    (back-to-back MMAs on one SM) measures here; the published HBM3e bandwidth."""
     import torch
+
+    import ring_attention_online_gb300 as ra
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    return {"tflops": sms * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12, "hbm_gbs": NOMINAL_HBM_GBS,
-            "basis": f"{sms} SMs x {mhz:.0f} MHz x {BF16_FLOP_PER_CLK_PER_SM} bf16 FLOP/clk/SM; HBM3e 7.9 TB/s"}
+    try:
+        cpm = ra.attn_probe_mma_cycles(4096)
+        rate, how = 128 * 128 * 16 * 2 / cpm, f"{cpm:.2f} cycles per 128x128x16 MMA, measured"
+    except Exception as e:  # the probe is a diagnostic: keep the documented rate
+        rate, how = float(BF16_FLOP_PER_CLK_PER_SM), f"probe failed ({e}); 64 cycles per MMA"
+    return {"tflops": sms * rate * mhz * 1e6 / 1e12, "hbm_gbs": NOMINAL_HBM_GBS,
+            "basis": f"{sms} SMs x {mhz:.0f} MHz x {rate:.0f} bf16 FLOP/clk/SM ({how}); HBM3e 7.9 TB/s"}
 
 
 def load_peaks():

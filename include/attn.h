@@ -228,6 +228,19 @@ attn_status_t attn_last_device_status(attn_stream_t stream);
  */
 attn_status_t attn_selftest_wait_timeout(uint64_t timeout_ns, attn_stream_t stream);
 
+/*
+ * attn_probe_mma_cycles - tensor-pipe rate probe.  One CTA issues groups x 8
+ * back-to-back tcgen05.mma kind::f16 M=128 N=128 K=16 MMAs from one thread (bf16
+ * operands in shared memory, fp32 accumulator in TMEM) and writes to cycles[0]
+ * the SM clock cycles from the first issue to the completion of the last, and to
+ * cycles[1] 0, or 1 if the bounded wait for that completion gave up.  cycles:
+ * device memory, 2 x uint64, 8-byte aligned, owned by the caller.  groups in
+ * [1, 1 << 20]; otherwise ATTN_ERR_INVALID_ARG.  128*128*16*2 / (cycles[0] /
+ * (8 * groups)) is the per-SM dense bf16 rate that the nominal roofline
+ * denominator is built from.  Has no counterpart on the pages.
+ */
+attn_status_t attn_probe_mma_cycles(unsigned long long* cycles, int groups, attn_stream_t stream);
+
 /* Static description of a status code; never NULL. */
 const char* attn_status_string(attn_status_t status);
 

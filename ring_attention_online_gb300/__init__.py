@@ -23,6 +23,7 @@ __all__ = [
     "attn_prefill", "attn_prefill_window", "attn_partial", "attn_merge", "attn_jagged", "attn_decode_splitkv",
     "attn_jagged_workspace_bytes", "attn_decode_workspace_bytes", "attn_decode_splitkv_noalloc",
     "attn_last_device_status", "attn_status_string", "attn_tile_walk", "attn_selftest_wait_timeout",
+    "attn_probe_mma_cycles",
     "BLOCK_M", "BLOCK_N", "STATUS",
 ]
 
@@ -61,6 +62,7 @@ _SIGNATURES = {
     "attn_prefill_window": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P],
     "attn_tile_walk": [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P],
     "attn_selftest_wait_timeout": [ctypes.c_uint64, _P],
+    "attn_probe_mma_cycles": [_P, _I, _P],
 }
 
 
@@ -226,6 +228,21 @@ def attn_selftest_wait_timeout(timeout_ns: int, stream=None):
     s = torch.cuda.current_stream() if stream is None else stream
     _check(load_library().attn_selftest_wait_timeout(int(timeout_ns), ctypes.c_void_p(s.cuda_stream)),
            "attn_selftest_wait_timeout")
+
+
+def attn_probe_mma_cycles(groups: int = 4096, stream=None) -> float:
+    """Cycles per tcgen05 kind::f16 M=128 N=128 K=16 MMA issued back to back on one SM
+    (see attn.h); the per-SM dense bf16 rate is 128*128*16*2 / this."""
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    out = torch.zeros(2, dtype=torch.int64, device=s.device)
+    _check(load_library().attn_probe_mma_cycles(ctypes.c_void_p(out.data_ptr()), int(groups),
+                                                ctypes.c_void_p(s.cuda_stream)), "attn_probe_mma_cycles")
+    s.synchronize()
+    cycles, gave_up = (int(x) for x in out.cpu().tolist())
+    if gave_up:
+        raise AttnError(4, "attn_probe_mma_cycles")
+    return cycles / (8.0 * int(groups))
 
 
 def attn_status_string(status: int) -> str:

@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 
 SOURCES = ["api.cu", "prefill_d64.cu", "prefill_d128.cu", "prefill_d256.cu", "merge.cu", "worklist.cu", "decode.cu",
-           "decode_noalloc.cu"]
+           "decode_noalloc.cu", "probe.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "schedule.cuh", "prefill_common.cuh", "prefill_kernel.cuh", "prefill_pair_kernel.cuh",
            "merge.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

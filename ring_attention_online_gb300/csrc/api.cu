@@ -321,6 +321,11 @@ attn_status_t attn_last_device_status(attn_stream_t stream) {
   return ATTN_OK;
 }
 
+attn_status_t attn_probe_mma_cycles(unsigned long long* cycles, int groups, attn_stream_t stream) {
+  if (!cycles || !aligned(cycles, 8) || groups < 1 || groups > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+  return launch_probe_mma(cycles, groups, reinterpret_cast<cudaStream_t>(stream));
+}
+
 attn_status_t attn_selftest_wait_timeout(uint64_t timeout_ns, attn_stream_t stream) {
   if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
   return launch_selftest_timeout(timeout_ns, reinterpret_cast<cudaStream_t>(stream));

@@ -71,6 +71,7 @@ attn_status_t launch_worklist(const int32_t* seq_offsets, int num_seqs, int tota
                               int block_m, int* count_and_items, int max_items, cudaStream_t s);
 unsigned int worklist_take_status(cudaStream_t s);
 attn_status_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t s);
+attn_status_t launch_probe_mma(unsigned long long* out, int groups, cudaStream_t s);
 
 // Split-KV decode partials; with `counters` (B * h_kv zeroed ints) the last
 // CTA of each (batch, KV head) also merges the partials into `out` and `lse`.

@@ -94,6 +94,13 @@ def test_partial_merge_jagged_decode_validation(lib):
                                    None) == 1
 
 
+def test_probe_validation(lib):
+    assert lib.attn_probe_mma_cycles(None, 16, None) == 1
+    assert lib.attn_probe_mma_cycles(ctypes.c_void_p(0x10004), 16, None) == 1  # not 8-byte aligned
+    assert lib.attn_probe_mma_cycles(FAKE, 0, None) == 1
+    assert lib.attn_probe_mma_cycles(FAKE, (1 << 20) + 1, None) == 1
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert ra.attn_status_string(code) != "unknown status"

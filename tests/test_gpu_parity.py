@@ -425,3 +425,12 @@ def test_malformed_offsets_reported_as_device_input_error():
     ra.attn_jagged(q, q, q, o, offs, 64, ws)
     assert ra.attn_last_device_status() == 5
     assert ra.attn_last_device_status() == 0
+
+
+# ---------------------------------------------------------------------- tensor-pipe probe
+def test_probe_mma_rate_matches_the_nominal_per_sm_rate():
+    """Back-to-back 128x128x16 bf16 MMAs on one SM issue every 64 cycles: 8192 FLOP per
+    cycle per SM, the figure the nominal roofline denominator is built from."""
+    cpm = ra.attn_probe_mma_cycles(2048)
+    assert 60.0 <= cpm <= 72.0, cpm
+    assert ra.attn_last_device_status() == 0
