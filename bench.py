@@ -265,6 +265,7 @@ def make_workload(name: str, device, batch=None, seq=None):
             pipe["started"] = True
             stream.wait_event(pipe["ev_out"][B - 1])  # the step ends with its last output on the host
         w["e2e_step"] = e2e_step
+        w["e2e_launches"] = cfg["B"]  # one prefill kernel per batch
     elif cfg["kind"] == "jagged":
         q, k, v, offs = syn.jagged_inputs(cfg, seed=0, device=device)
         T = int(offs[-1])
@@ -471,8 +472,11 @@ def run_ours(args):
         units_e2e, ms_e2e_max = aggregate(w["units"] * K2, ms_e2e, world, device)
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
+        e2e_launches = K2 * w.get("e2e_launches", w["launches"])
         line["e2e"] = {"value": round(units_e2e / (ms_e2e_max / 1e3), 2), "unit": w["unit"],
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2}
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2,
+                       "gpu_launches": e2e_launches}
+        line["gpu_launches"] += e2e_launches
         del host_in, host_out
     del w
     torch.cuda.empty_cache()
