@@ -363,229 +363,229 @@ __global__ void __launch_bounds__(352, 1)
     int gj = 0;    // tiles so far, all items: the phases of the per-tile barriers
     int n_ep = 0;  // epilogues so far
     for (int i = 0; ok && i < n_my; ++i) {
-    const Item it = get_item(i);
-    TileWalk sw_walk;
-    const int n = item_walk(it, sw_walk);
-    const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
-    const int q_row = q_lo + row;
-    float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
-    float l_run = 0.f;             // this half's sum of exp2(x - m_run) in fp32: l and LSE
-    float lr_run = 0.f;            // this half's sum of the rounded P the MMA multiplies V by
-    float m_max = -CUDART_INF_F;   // true running max (partial mode)
-    for (int j = 0; j < n; ++j, ++gj) {
-      int ch, kstart, mend;
-      sw_walk.next(ch, kstart, mend);
-      const int buf = gj & 1;
-      if (!pf_wait_outlined(&bar_s[buf], (uint32_t)((gj >> 1) & 1), &abort_flag, 6)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(lane_addr + half * 64, r0);
-      tmem_ld32(lane_addr + half * 64 + 32, r1);
-      tmem_ld_wait(r0);
-      tmem_ld_wait(r1);
-      // S(j) is in registers: the S issuer may overwrite the buffer with S(j+1)
-      tc_fence_before_sync();
-      mbar_arrive(&bar_sfree[buf]);
-
-      // mask the diagonal / tail tile (key kstart + i is visible iff i < lim)
-      // and, under a sliding window, the tiles at its lower edge (iff i >= flo)
-      constexpr bool win = kMode == kModeWindow;
-      const bool need_mask =
-          (kstart + C::BN > mend) ||
-          (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo)) ||
-          (win && (long long)kv_pos0 + kstart < (long long)q_pos0 + q_hi - 1 - p.window);
-      if (need_mask) {
-        long long lim = (long long)mend - kstart;
-        long long flo = 0;
-        if (p.causal) {
-          const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
-          lim = lc < lim ? lc : lim;
-          if (win) flo = lc - 1 - p.window;
-        }
-        const long long lh = lim - half * 64, fh = flo - half * 64;  // limits within this half
-        const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (i >= lh || i < fh) r0[i] = ninf;
-          if (i + 32 >= lh || i + 32 < fh) r1[i] = ninf;
-        }
-      }
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        mx8[i] = fmax3(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8]), __uint_as_float(r0[i + 16]));
-        mx8[i] = fmax3(mx8[i], __uint_as_float(r0[i + 24]), __uint_as_float(r1[i]));
-        mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 8]), __uint_as_float(r1[i + 16]));
-        mx8[i] = fmaxf(mx8[i], __uint_as_float(r1[i + 24]));
-      }
-      float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      // both halves of the row see each other's max
-      xch_max[buf][half][row] = mx;
-      mbar_arrive(&bar_x[buf][wq]);
-      if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((gj >> 1) & 1), &abort_flag, 9)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, xch_max[buf][half ^ 1][row]);
-      const float m_tile = mx * c;  // -inf when the whole row is masked
-      if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
-      const float m_new = fmaxf(m_run, m_tile);
-      const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
-      float alpha = 1.f;
-      if (raise) {
-        alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
-        m_run = m_new;
-        l_run *= alpha;
-        lr_run *= alpha;
-      }
-      // P goes to P buffer gj % 2, which the PV two tiles back read; that PV is
-      // waited for here and so always before this tile's PV is issued (no
-      // waiter falls two phases behind on bar_o)
-      if (gj >= 2) {
-        if (!pf_wait_outlined(&bar_o[buf], (uint32_t)(((gj - 2) >> 1) & 1), &abort_flag, 12)) {
+      const Item it = get_item(i);
+      TileWalk sw_walk;
+      const int n = item_walk(it, sw_walk);
+      const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
+      const int q_row = q_lo + row;
+      float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
+      float l_run = 0.f;             // this half's sum of exp2(x - m_run) in fp32: l and LSE
+      float lr_run = 0.f;            // this half's sum of the rounded P the MMA multiplies V by
+      float m_max = -CUDART_INF_F;   // true running max (partial mode)
+      for (int j = 0; j < n; ++j, ++gj) {
+        int ch, kstart, mend;
+        sw_walk.next(ch, kstart, mend);
+        const int buf = gj & 1;
+        if (!pf_wait_outlined(&bar_s[buf], (uint32_t)((gj >> 1) & 1), &abort_flag, 6)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-      }
-      const uint32_t pcol = lane_addr + C::P_COL + static_cast<uint32_t>(buf * 64);
-      const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
-      const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
-      uint64_t sum2 = f2_make(0.f, 0.f);
-      float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // rounded weights, 8 chains
-      uint32_t pk[16];
-      auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 e = f2_split(f2_fma(f2_make_u(r[2 * i], r[2 * i + 1]), c2, nm2));
-          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
-          pk[i] = pack_half2<kBf16>(p0, p1);
-          sum2 = f2_add(sum2, f2_make(p0, p1));
-          // O is normalised by the sum of the rounded weights it was built
-          // from, so O / l is a weighted mean with consistent weights
-          add_half2_to_f32<kBf16>(sr[2 * (i & 3)], sr[2 * (i & 3) + 1], pk[i]);
-        }
-        tmem_st16(pcol + col, pk);
-      };
-      // P(j) for keys [64*half, 64*half+64) goes to its columns [32*half, 32*half+32)
-      pack_chunk(r0, half * 32);
-      pack_chunk(r1, half * 32 + 16);
-      const float2 sv = f2_split(sum2);
-      l_run += sv.x + sv.y;
-      lr_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+        uint32_t r0[32], r1[32];
+        tmem_ld32(lane_addr + half * 64, r0);
+        tmem_ld32(lane_addr + half * 64 + 32, r1);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        // S(j) is in registers: the S issuer may overwrite the buffer with S(j+1)
+        tc_fence_before_sync();
+        mbar_arrive(&bar_sfree[buf]);
 
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        // the previous PV must be complete before O is rescaled.  The PV before
-        // it, on the same barrier, was waited for above one tile ago, so this
-        // wait is never more than one phase behind, and tiles that need no
-        // rescale need not wait.
-        if (!pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 7)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll 1
-        for (int cc = 0; cc < HD / 32; ++cc) {
-          uint32_t o[32];
-          const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
-          tmem_ld32(oa, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(oa, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&bar_p[buf]);
-    }
-    if (ok && n > 0) {
-      // the item's last P.V (the earlier ones are done or finish before it)
-      ok = pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8);
-      tc_fence_after_sync();
-    }
-    // the row's sums are split over the two halves (one exchange buffer per
-    // item parity: a half cannot get two epilogues ahead of its partner)
-    const int ep = n_ep & 1;
-    xch_l[ep][half][row] = l_run;
-    xch_lr[ep][half][row] = lr_run;
-    mbar_arrive(&bar_xe[wq]);
-    if (ok) ok = pf_wait_outlined(&bar_xe[wq], (uint32_t)ep, &abort_flag, 10);
-    ++n_ep;
-    l_run += xch_l[ep][half ^ 1][row];
-    lr_run += xch_lr[ep][half ^ 1][row];
-    if (ok) {
-      const bool row_valid = q_row < q_hi;
-      const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
-      const size_t lse_idx = ((size_t)b * p.h_q + h) * p.S_q + q_row;
-      constexpr float kLn2 = 0.693147180559945309f;
-      if constexpr (kMode != kModePartial) {
-        const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
-        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + half * HD;
-        const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
-#pragma unroll 1
-        for (int cc = 0; cc < HD / 32; ++cc) {
-          uint32_t o[32];
-          if (n > 0) {
-            tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
-            tmem_ld_wait(o);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
+        // mask the diagonal / tail tile (key kstart + i is visible iff i < lim)
+        // and, under a sliding window, the tiles at its lower edge (iff i >= flo)
+        constexpr bool win = kMode == kModeWindow;
+        const bool need_mask =
+            (kstart + C::BN > mend) ||
+            (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo)) ||
+            (win && (long long)kv_pos0 + kstart < (long long)q_pos0 + q_hi - 1 - p.window);
+        if (need_mask) {
+          long long lim = (long long)mend - kstart;
+          long long flo = 0;
+          if (p.causal) {
+            const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
+            lim = lc < lim ? lc : lim;
+            if (win) flo = lc - 1 - p.window;
           }
-          uint32_t w[16];
+          const long long lh = lim - half * 64, fh = flo - half * 64;  // limits within this half
+          const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (row_valid) {
-            // a warp's store touches 32 rows: 32-byte pieces halve the requests
-            // of 16-byte ones (the output's base decides)
-            if (o_v8) {
-              st_global_v8(orow + cc * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-              st_global_v8(orow + cc * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+          for (int i = 0; i < 32; ++i) {
+            if (i >= lh || i < fh) r0[i] = ninf;
+            if (i + 32 >= lh || i + 32 < fh) r1[i] = ninf;
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mx8[i] = fmax3(__uint_as_float(r0[i]), __uint_as_float(r0[i + 8]), __uint_as_float(r0[i + 16]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r0[i + 24]), __uint_as_float(r1[i]));
+          mx8[i] = fmax3(mx8[i], __uint_as_float(r1[i + 8]), __uint_as_float(r1[i + 16]));
+          mx8[i] = fmaxf(mx8[i], __uint_as_float(r1[i + 24]));
+        }
+        float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        // both halves of the row see each other's max
+        xch_max[buf][half][row] = mx;
+        mbar_arrive(&bar_x[buf][wq]);
+        if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((gj >> 1) & 1), &abort_flag, 9)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, xch_max[buf][half ^ 1][row]);
+        const float m_tile = mx * c;  // -inf when the whole row is masked
+        if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
+        float alpha = 1.f;
+        if (raise) {
+          alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
+          m_run = m_new;
+          l_run *= alpha;
+          lr_run *= alpha;
+        }
+        // P goes to P buffer gj % 2, which the PV two tiles back read; that PV is
+        // waited for here and so always before this tile's PV is issued (no
+        // waiter falls two phases behind on bar_o)
+        if (gj >= 2) {
+          if (!pf_wait_outlined(&bar_o[buf], (uint32_t)(((gj - 2) >> 1) & 1), &abort_flag, 12)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        const uint32_t pcol = lane_addr + C::P_COL + static_cast<uint32_t>(buf * 64);
+        const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+        const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
+        uint64_t sum2 = f2_make(0.f, 0.f);
+        float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // rounded weights, 8 chains
+        uint32_t pk[16];
+        auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 e = f2_split(f2_fma(f2_make_u(r[2 * i], r[2 * i + 1]), c2, nm2));
+            const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+            pk[i] = pack_half2<kBf16>(p0, p1);
+            sum2 = f2_add(sum2, f2_make(p0, p1));
+            // O is normalised by the sum of the rounded weights it was built
+            // from, so O / l is a weighted mean with consistent weights
+            add_half2_to_f32<kBf16>(sr[2 * (i & 3)], sr[2 * (i & 3) + 1], pk[i]);
+          }
+          tmem_st16(pcol + col, pk);
+        };
+        // P(j) for keys [64*half, 64*half+64) goes to its columns [32*half, 32*half+32)
+        pack_chunk(r0, half * 32);
+        pack_chunk(r1, half * 32 + 16);
+        const float2 sv = f2_split(sum2);
+        l_run += sv.x + sv.y;
+        lr_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // the previous PV must be complete before O is rescaled.  The PV before
+          // it, on the same barrier, was waited for above one tile ago, so this
+          // wait is never more than one phase behind, and tiles that need no
+          // rescale need not wait.
+          if (!pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 7)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
+            tmem_ld32(oa, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(oa, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bar_p[buf]);
+      }
+      if (ok && n > 0) {
+        // the item's last P.V (the earlier ones are done or finish before it)
+        ok = pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8);
+        tc_fence_after_sync();
+      }
+      // the row's sums are split over the two halves (one exchange buffer per
+      // item parity: a half cannot get two epilogues ahead of its partner)
+      const int ep = n_ep & 1;
+      xch_l[ep][half][row] = l_run;
+      xch_lr[ep][half][row] = lr_run;
+      mbar_arrive(&bar_xe[wq]);
+      if (ok) ok = pf_wait_outlined(&bar_xe[wq], (uint32_t)ep, &abort_flag, 10);
+      ++n_ep;
+      l_run += xch_l[ep][half ^ 1][row];
+      lr_run += xch_lr[ep][half ^ 1][row];
+      if (ok) {
+        const bool row_valid = q_row < q_hi;
+        const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
+        const size_t lse_idx = ((size_t)b * p.h_q + h) * p.S_q + q_row;
+        constexpr float kLn2 = 0.693147180559945309f;
+        if constexpr (kMode != kModePartial) {
+          const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + half * HD;
+          const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            if (n > 0) {
+              tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
+              tmem_ld_wait(o);
             } else {
-              uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4)
-                dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_half2<kBf16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (row_valid) {
+              // a warp's store touches 32 rows: 32-byte pieces halve the requests
+              // of 16-byte ones (the output's base decides)
+              if (o_v8) {
+                st_global_v8(orow + cc * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                st_global_v8(orow + cc * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                  dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+              }
             }
           }
-        }
-        if (p.lse != nullptr && row_valid && half == 0)
-          p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
-      } else {
-        const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
-        const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
-        // O re-weighted so that O / l equals the consistently normalised O_acc / lr
-        const float fo = any ? f * (l_run / lr_run) : 0.f;
-        float* orow = p.o_part + row_idx * D + half * HD;
+          if (p.lse != nullptr && row_valid && half == 0)
+            p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
+        } else {
+          const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
+          const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
+          // O re-weighted so that O / l equals the consistently normalised O_acc / lr
+          const float fo = any ? f * (l_run / lr_run) : 0.f;
+          float* orow = p.o_part + row_idx * D + half * HD;
 #pragma unroll 1
-        for (int cc = 0; cc < HD / 32; ++cc) {
-          uint32_t o[32];
-          if (n > 0) {
-            tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
-            tmem_ld_wait(o);
-          } else {
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            if (n > 0) {
+              tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
+              tmem_ld_wait(o);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-          }
-          if (row_valid) {
-            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            if (row_valid) {
+              float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
-                                    __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
+                                      __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+            }
           }
-        }
-        if (row_valid && half == 0) {
-          p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
-          p.l_out[lse_idx] = any ? l_run * f : 0.f;
+          if (row_valid && half == 0) {
+            p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
+            p.l_out[lse_idx] = any ? l_run * f : 0.f;
+          }
         }
       }
-    }
     }  // items
   }
 
