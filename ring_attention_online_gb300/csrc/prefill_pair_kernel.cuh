@@ -82,8 +82,8 @@ __device__ __forceinline__ int pair_item_count(const PrefillParams& p) {
 }
 
 // Work unit k: items [i0, i0 + n) of head h.  A jagged unit is every Q tile of
-// one (sequence, head), taken back to back by one CTA so that the sequence's
-// K/V, read by its first (longest) tile, is re-read from L2 by the others
+// one (sequence, head), first to last, taken back to back by one CTA so that
+// each tile re-reads from L2 the K/V its predecessors brought in
 // ("Grouping" in "[pallas] Support dependent Tile.end bounds in Pallas":
 // successive Q work items reuse the resident K/V range).  The worklist's item
 // count bounds the unit's items.

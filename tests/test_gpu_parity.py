@@ -256,12 +256,12 @@ def test_jagged_parity_and_worklist(causal, D):
     got = sorted(map(tuple, items.tolist()))
     want = sorted((it["ordered_begin"], it["range_len"], it["tile_start"], it["tile_extent"]) for it in ref)
     assert got == want
-    # order: non-increasing Q-tile count per sequence, and each sequence's tiles last-to-first
+    # order: non-increasing Q-tile count per sequence, and each sequence's tiles first-to-last
     ntiles = [(r[1] + block_m - 1) // block_m for r in items]
     assert all(a >= b for a, b in zip(ntiles, ntiles[1:]))
     for a, b in zip(items, items[1:]):
         if a[0] == b[0]:
-            assert b[2] == a[2] - block_m
+            assert b[2] == a[2] + block_m
     # units: one per non-empty sequence, covering its contiguous items in order
     n_units = int(words[1])
     max_items = (int(offs[-1]) + (len(offs) - 1) * (block_m - 1)) // block_m
