@@ -70,13 +70,16 @@ dim3 persistent_grid(long long items) {
 }
 
 // Fills the work-item decomposition of the paired kernel and its grid (one
-// item per CTA); the single-tile kernel takes one CTA per (Q tile, head,
-// batch).  False when the item count does not fit a 32-bit item index.
+// item per CTA); the single-tile kernel runs one CTA per SM over units of two
+// Q tiles of one (batch, head).  False when the item count does not fit a
+// 32-bit item index.
 bool dense_grid(PrefillParams& p, int D, dim3* grid) {
   if (!paired(D)) {
-    // two Q tiles per CTA (see prefill_kernel.cuh)
+    // persistent over units of two Q tiles (see prefill_kernel.cuh)
     const int n_qt = (p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M;
-    *grid = dim3((n_qt + 1) / 2, p.h_q, p.B);
+    const long long units = (long long)((n_qt + 1) / 2) * p.h_q * p.B;
+    if (2 * ((units + sm_count() - 1) / sm_count()) > 0x7fffffffLL) return false;
+    *grid = persistent_grid(units);
     return true;
   }
   const int rows = p.pair_heads ? ATTN_BLOCK_M : 2 * ATTN_BLOCK_M;

@@ -1,5 +1,5 @@
 // Blockwise online-softmax attention forward, tcgen05 + TMA, Q tiles of 128
-// rows, two per CTA for dense launches.
+// rows, persistent over units of two for dense launches.
 //
 // What it computes, by source:
 //  * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel: per KV block,
@@ -12,14 +12,15 @@
 //    at min(kv_end, tile_q.end) (no fully masked tile is visited); only the
 //    diagonal and tail tiles are masked.
 //
-// Work: a dense, partial or window CTA takes two Q tiles of one (batch,
-// head), t and n_qt - 1 - t when causal (so every CTA walks n_qt + 1 KV
-// tiles) or 2x and 2x + 1 otherwise, the longer first; a jagged CTA takes one
-// worklist item.  Barrier phases and the K/V stage ring run on from the first
-// item to the second, so the second item's Q and first K/V tiles load, and its
-// first S is computed, while the first item's last tiles and epilogue finish:
-// a CTA's fixed costs (start-up, first loads, pipeline fill) were ~11 K cycles
-// per Q tile, 18 % of the dense causal S=4096 launch.
+// Work: dense, partial and window launches run one CTA per SM over units of
+// two Q tiles of one (batch, head), t and n_qt - 1 - t when causal (so every
+// unit walks n_qt + 1 KV tiles) or 2x and 2x + 1 otherwise, the longer first;
+// a jagged CTA takes one worklist item.  Barrier phases and the K/V stage ring
+// run on across all of a CTA's items, so each item's Q and first K/V tiles
+// load, and its first S is computed, while the previous item's last tiles and
+// epilogue finish: with one CTA per Q tile, a CTA's fixed costs (start-up,
+// first loads, pipeline fill and drain) were ~11 K cycles, 18 % of the dense
+// causal S=4096 launch.
 //
 // CTA layout (352 threads):
 //   warp 0      TMA producer: per item the Q tile (once the previous item's S
@@ -96,28 +97,34 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ uint64_t bar_xe[4];         // end-of-row exchange barrier per lane quarter
 
   // ------------------------------------------------------------ work items
+  // Dense / window / partial launches are persistent: CTA c takes the units
+  // c, c + grid, c + 2 grid, ... in the order (pair x, head, batch), so the
+  // CTAs running at one time share the K/V of a few heads in L2.  A unit is
+  // two Q tiles of one (batch, head), t and n_qt - 1 - t when causal (every
+  // unit then walks n_qt + 1 KV tiles; the longer first), 2x and 2x + 1
+  // otherwise; its second slot is empty when the two coincide or the second
+  // lies past the end.  Barrier phases and the stage ring run on across all of
+  // a CTA's items, so each item's Q and first K/V tiles load, and its first S
+  // is computed, while the previous item finishes.  One CTA per unit (the
+  // hardware's launch order) measured 4 % slower: the CTA start-up and
+  // pipeline fill and drain were exposed once per unit.  Jagged launches take
+  // one worklist item per CTA.
   struct Item {
     int b, h, q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0;
+    bool valid;
   };
-  int n_my = 1;  // items of this CTA
-  int t_first = 0, t_second = 0;
+  const int n_qt = (p.S_q + C::BM - 1) / C::BM;
+  const int n_ux = (n_qt + 1) / 2;  // units per (batch, head)
+  int n_my = 1;                     // item slots of this CTA
   if constexpr (kMode == kModeJagged) {
     if ((int)blockIdx.x >= *p.work_count) return;  // the grid is an upper bound on the item count
   } else {
-    const int n_qt = (p.S_q + C::BM - 1) / C::BM;
-    const int x = (int)blockIdx.x;
-    if (p.causal) {
-      t_first = n_qt - 1 - x;
-      t_second = x;
-      n_my = t_second < t_first ? 2 : 1;
-    } else {
-      t_first = 2 * x;
-      t_second = 2 * x + 1;
-      n_my = t_second < n_qt ? 2 : 1;
-    }
+    const long long units = (long long)n_ux * p.h_q * p.B;
+    n_my = 2 * (int)((units - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x);
   }
   auto get_item = [&](int i) -> Item {
     Item it;
+    it.valid = true;
     if constexpr (kMode == kModeJagged) {
       (void)i;
       const int4 w = p.work_items[blockIdx.x];
@@ -130,9 +137,20 @@ __global__ void __launch_bounds__(352, 1)
       it.q_pos0 = 0;
       it.kv_pos0 = 0;
     } else {
-      const int qt = i == 0 ? t_first : t_second;
-      it.b = blockIdx.z;
-      it.h = blockIdx.y;
+      const long long u = (long long)blockIdx.x + (long long)(i >> 1) * gridDim.x;
+      const int x = (int)(u % n_ux);
+      const long long yb = u / n_ux;
+      int qt;
+      if (p.causal) {
+        const int t_first = n_qt - 1 - x;
+        qt = (i & 1) ? x : t_first;
+        it.valid = !(i & 1) || x < t_first;
+      } else {
+        qt = 2 * x + (i & 1);
+        it.valid = qt < n_qt;
+      }
+      it.b = (int)(yb / p.h_q);
+      it.h = (int)(yb % p.h_q);
       it.q_lo = qt * C::BM;
       it.q_hi = min(it.q_lo + C::BM, p.S_q);
       it.kv_lo = p.kv_lo;
@@ -147,7 +165,7 @@ __global__ void __launch_bounds__(352, 1)
            kMode == kModeWindow ? p.window : -1);
     return w.count();
   };
-  const int hk = (int)blockIdx.y / p.group;
+  int hk = (int)blockIdx.y / p.group;  // the producer's KV head, set per item
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -212,6 +230,8 @@ __global__ void __launch_bounds__(352, 1)
       };
       for (int i = 0; ok && i < n_my; ++i) {
         const Item it = get_item(i);
+        if (!it.valid) continue;
+        hk = it.h / p.group;
         TileWalk walk;
         const int n = item_walk(it, walk);
         if (n == 0) continue;
@@ -280,6 +300,7 @@ __global__ void __launch_bounds__(352, 1)
       int q_used = 0;     // Q tiles consumed (S issuer)
       for (int i = 0; ok && i < n_my; ++i) {
         const Item it = get_item(i);
+        if (!it.valid) continue;
         TileWalk walk;
         const int n = item_walk(it, walk);
         if (n == 0) continue;
@@ -364,6 +385,7 @@ __global__ void __launch_bounds__(352, 1)
     int n_ep = 0;  // epilogues so far
     for (int i = 0; ok && i < n_my; ++i) {
       const Item it = get_item(i);
+      if (!it.valid) continue;
       TileWalk sw_walk;
       const int n = item_walk(it, sw_walk);
       const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
