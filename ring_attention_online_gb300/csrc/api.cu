@@ -154,6 +154,8 @@ attn_status_t prefill_impl(const void* q, const void* k, const void* v, void* o,
     return ATTN_ERR_CUDA;
   dim3 grid;
   if (!dense_grid(p, D, &grid)) return ATTN_ERR_UNSUPPORTED;
+  // the paired kernel's window launches are persistent over its items
+  if (paired(D) && window >= 0) grid = persistent_grid(p.n_items);
   return launch_prefill(p, mq, mk, mv, window >= 0 ? kModeWindow : kModeDense, bf16, D, grid,
                         reinterpret_cast<cudaStream_t>(stream));
 }
