@@ -115,6 +115,46 @@ def test_prefill_window_ring_gqa(C):
     close_lse(lse, L)
 
 
+# ---------------------------------------------------------------------- persistent grids
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_d256_persistent_many_units(causal):
+    """Head dim 256 runs one CTA per SM over units of two Q tiles: here there are more
+    than twice as many units as SMs, so every CTA chains several, and the odd Q-tile
+    count gives every (batch, head) a unit with an empty second slot (the causal middle
+    tile, the non-causal last one)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, S_, h_q, h_kv, D = 4, 300, 48, 8, 256
+    units = B * h_q * (((S_ + 127) // 128 + 1) // 2)
+    assert units > 2 * sms
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=60 + causal)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill(q, k, v, o, lse, causal=causal)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), causal)
+    close_o(o, O, f"persistent D=256 causal={causal}")
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("C", [1, 3])
+@pytest.mark.parametrize("D,h_q,h_kv", [(128, 16, 8), (64, 12, 12)])
+def test_prefill_window_persistent_many_items(D, h_q, h_kv, C):
+    """Sliding-window launches of the paired kernel are persistent (items in a snake
+    order over one CTA per SM): more items than SMs, as head pairs (GQA) and as Q-tile
+    pairs, with a ragged last tile, in one chunk and in a three-chunk ring walk."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, S_, window = 3, 1100, 300
+    rows = 128 if (h_q // h_kv) % 2 == 0 else 256
+    items = B * ((S_ + rows - 1) // rows) * (h_q // 2 if rows == 128 else h_q)
+    assert items > sms
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=70 + D)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill_window(q, k, v, o, lse, window=window, num_chunks=C)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), True, window=window)
+    close_o(o, O, f"persistent window D={D} C={C}")
+    close_lse(lse, L)
+
+
 @pytest.mark.parametrize("S_q,S_kv", [(200, 700), (700, 200), (1, 513), (129, 1)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_prefill_unequal_lengths(S_q, S_kv, causal):
