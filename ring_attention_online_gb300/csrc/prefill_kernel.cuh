@@ -15,7 +15,7 @@
 // Work: dense, partial and window launches run one CTA per SM over units of
 // two Q tiles of one (batch, head), t and n_qt - 1 - t when causal (so every
 // unit walks n_qt + 1 KV tiles) or 2x and 2x + 1 otherwise, the longer first;
-// a jagged CTA takes one worklist item.  Barrier phases and the K/V stage ring
+// a jagged CTA takes one worklist item.  Barrier phases and the K/V stage rings
 // run on across all of a CTA's items, so each item's Q and first K/V tiles
 // load, and its first S is computed, while the previous item's last tiles and
 // epilogue finish: with one CTA per Q tile, a CTA's fixed costs (start-up,
@@ -25,8 +25,8 @@
 // CTA layout (352 threads):
 //   warp 0      TMA producer: per item the Q tile (once the previous item's S
 //               MMAs are done with the Q buffer), then K/V 128-column slabs
-//               through a ring of NST shared-memory stages: K(0), then per
-//               tile K(j+1), V(j).
+//               through a K ring and a V ring of shared-memory stages, in
+//               the order K(0), then per tile K(j+1), V(j).
 //   warp 1      TMEM owner and S issuer: S(j) = Q.K_j^T into the one
 //               128-column S buffer, once the softmax warps have read S(j-1)
 //               out of it.
@@ -61,8 +61,13 @@ struct PrefillCfg {
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int SLAB_BYTES = BN * SC * 2;
   // four K/V slabs in flight: on GB300 two to six stages time the same, so
-  // the rest of shared memory stays free for the softmax warps' exchanges
+  // the rest of shared memory stays free for the softmax warps' exchanges.
+  // K and V have rings of their own (NST / 2 stages each, K first), so each
+  // stage's fills are consumed by one issuer in order: a consumer never waits
+  // on a fill while the stage's previous one is still pending, which the
+  // parity wait of an mbarrier could not tell from a completed one
   static constexpr int NST = D == 64 ? 8 : 4;
+  static constexpr int RING = NST / 2;  // stages per ring
   static constexpr int SMEM_BYTES = Q_BYTES + NST * SLAB_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM: S(j) in columns [0, 128) (one buffer); P(j) (bf16/fp16, 64 columns)
@@ -71,7 +76,7 @@ struct PrefillCfg {
   static constexpr uint32_t O_COL = 256;
   static constexpr int THREADS = 352;  // TMA warp, S issuer, 8 softmax warps, PV issuer
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
-  static_assert(NST >= 2, "at least two K/V stages");
+  static_assert(NST >= 2 && NST % 2 == 0, "K and V rings of equal size");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(352, 1)
   // two Q tiles of one (batch, head), t and n_qt - 1 - t when causal (every
   // unit then walks n_qt + 1 KV tiles; the longer first), 2x and 2x + 1
   // otherwise; its second slot is empty when the two coincide or the second
-  // lies past the end.  Barrier phases and the stage ring run on across all of
+  // lies past the end.  Barrier phases and the stage rings run on across all of
   // a CTA's items, so each item's Q and first K/V tiles load, and its first S
   // is computed, while the previous item finishes.  One CTA per unit (the
   // hardware's launch order) measured 4 % slower: the CTA start-up and
@@ -208,23 +213,21 @@ __global__ void __launch_bounds__(352, 1)
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
+      int filled[2] = {0, 0};  // slabs issued into the K ring and the V ring
       int q_loads = 0;
       bool ok = true;
-      auto push = [&](const CUtensorMap* map, int start, int bb) -> bool {
-        for (int hs = 0; hs < C::NH; ++hs) {
+      // fill f of a ring goes to its stage f % RING; fill f - RING of that
+      // stage must have been released by its issuer first
+      auto push = [&](const CUtensorMap* map, int start, int bb, int ring) -> bool {
+        int& fills = filled[ring];
+        for (int hs = 0; hs < C::NH; ++hs, ++fills) {
+          const int stage = ring * C::RING + fills % C::RING;
+          const uint32_t phase = (uint32_t)((fills / C::RING) & 1);
           if (!pf_wait_outlined(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
           uint8_t* dst = sKV + stage * C::SLAB_BYTES;
           mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
           for (int blk = 0; blk < C::BLK_PER_SLAB; ++blk)
             tma_load_4d(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], hs * C::SC + blk * 64, hk, start, bb);
-          ++issued;
-          if (++stage == C::NST) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
         return true;
       };
@@ -247,24 +250,26 @@ __global__ void __launch_bounds__(352, 1)
         TileWalk kw = walk, vw = walk;
         int ch, st, me;
         kw.next(ch, st, me);
-        ok = push(&mk, st, it.b);
+        ok = push(&mk, st, it.b, 0);
         for (int j = 0; ok && j < n; ++j) {
           if (j + 1 < n) {
             kw.next(ch, st, me);
-            ok = push(&mk, st, it.b);
+            ok = push(&mk, st, it.b, 0);
             if (!ok) break;
           }
           vw.next(ch, st, me);
-          ok = push(&mv, st, it.b);
+          ok = push(&mv, st, it.b, 1);
         }
       }
       if (abort_flag) {
         // copies may still be landing in shared memory: wait for them
         if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
-        const int outstanding = issued < C::NST ? issued : C::NST;
-        for (int i = 0; i < outstanding; ++i) {
-          const int pos = issued - 1 - i;
-          pf_drain(&bar_full[pos % C::NST], (uint32_t)((pos / C::NST) & 1));
+        for (int ring = 0; ring < 2; ++ring) {
+          const int outstanding = filled[ring] < C::RING ? filled[ring] : C::RING;
+          for (int i = 0; i < outstanding; ++i) {
+            const int pos = filled[ring] - 1 - i;
+            pf_drain(&bar_full[ring * C::RING + pos % C::RING], (uint32_t)((pos / C::RING) & 1));
+          }
         }
       }
     }
@@ -281,22 +286,21 @@ __global__ void __launch_bounds__(352, 1)
       constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, kBf16, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32acc(128, C::SC, kBf16, true);
       const uint32_t skv = smem_u32(sKV);
-      // stage order of the producer within an item: K(0), then per tile
-      // K(j+1), V(j); in tiles of NH slabs, K(j) is tile 2j - 1 (j > 0) and
-      // V(j) tile 2j + 2, except V(n - 1), the last tile, 2n - 1; an item's
-      // 2n tiles follow the previous item's in the ring
-      auto k_tile = [](int j) { return j == 0 ? 0 : 2 * j - 1; };
-      auto v_tile = [](int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; };
-      // each slab is waited for right before its MMAs, so the first half of S(j)
-      // (PV(j)) can run while the second half's K (V) is still landing
-      auto wait_slab = [&](int s, uint32_t site) -> bool {
-        if (!pf_wait_outlined(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, site)) return false;
+      // the S issuer takes every K slab, the PV issuer every V slab, each in
+      // the order the producer filled its ring: slab f of a ring is in stage
+      // ring * RING + f % RING, fill parity (f / RING) & 1.  Each slab is waited
+      // for right before its MMAs, so the first half of S(j) (PV(j)) can run
+      // while the second half's K (V) is still landing
+      auto wait_slab = [&](int ring, int f, uint32_t site) -> bool {
+        if (!pf_wait_outlined(&bar_full[ring * C::RING + f % C::RING], (uint32_t)((f / C::RING) & 1), &abort_flag,
+                              site))
+          return false;
         tc_fence_after_sync();
         return true;
       };
       bool ok = true;
       int g = 0;          // S (or PV) groups issued so far, all items: its barrier phases
-      int slab_base = 0;  // first slab of the current item
+      int slab_base = 0;  // slabs of this issuer's ring taken by the earlier items
       int q_used = 0;     // Q tiles consumed (S issuer)
       for (int i = 0; ok && i < n_my; ++i) {
         const Item it = get_item(i);
@@ -316,12 +320,11 @@ __global__ void __launch_bounds__(352, 1)
               if (!ok) break;
               tc_fence_after_sync();
             }
-            const int kt = k_tile(j);
             const uint32_t d_tmem = tmem;
             for (int hs = 0; hs < C::NH; ++hs) {
-              const int sl = slab_base + kt * C::NH + hs;
-              const int stage = sl % C::NST;
-              ok = wait_slab(sl, 2);
+              const int sl = slab_base + j * C::NH + hs;
+              const int stage = sl % C::RING;  // K ring
+              ok = wait_slab(0, sl, 2);
               if (!ok) break;
               const uint64_t kdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16, 1024);
 #pragma unroll
@@ -341,14 +344,13 @@ __global__ void __launch_bounds__(352, 1)
           for (int j = 0; ok && j < n; ++j, ++g) {
             ok = pf_wait_outlined(&bar_p[g & 1], (uint32_t)((g >> 1) & 1), &abort_flag, 3);
             if (!ok) break;
-            const int vt = v_tile(j, n);
             tc_fence_after_sync();  // P in TMEM
             const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((g & 1) * 64);
             const uint32_t acc0 = j > 0 ? 1u : 0u;  // the item's first PV starts O afresh
             for (int hs = 0; hs < C::NH; ++hs) {
-              const int sl = slab_base + vt * C::NH + hs;
-              const int stage = sl % C::NST;
-              ok = wait_slab(sl, 4);
+              const int sl = slab_base + j * C::NH + hs;
+              const int stage = C::RING + sl % C::RING;  // V ring
+              ok = wait_slab(1, sl, 4);
               if (!ok) break;
               const uint64_t vdesc = smem_desc_sw128(skv + stage * C::SLAB_BYTES, 16384, 1024);
 #pragma unroll
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(352, 1)
             mma_commit(&bar_o[g & 1]);
           }
         }
-        slab_base += 2 * n * C::NH;
+        slab_base += n * C::NH;
       }
       // every MMA either issuer issued must finish before TMEM is released
       mma_commit(&bar_fin);
