@@ -355,33 +355,41 @@ def tensor_roofline(w, kernel_ms_per_launch: float, peaks, peak_kind: str, nomin
 
 
 # ------------------------------------------------------------------ CPU legs (oracle)
-def cpu_sample_dense(seconds: float, rows_per_sample: int = 512):
-    """fp64 oracle on query-row blocks of the headline workload (host cores)."""
-    import numpy as np
+def _cpu_slice():
+    """One (batch, head) slice of the headline workload, drawn with its recipe (host)."""
     import torch
-
-    import synthetic as syn
-    from oracle import attention as A
-    cfg = syn.WORKLOADS[HEADLINE]
+    cfg = __import__("synthetic").WORKLOADS[HEADLINE]
     S, D = cfg["S_q"], cfg["D"]
     gen = torch.Generator().manual_seed(0)
-    # one (batch, head) slice of the workload at a time, drawn with the same recipe
+    return tuple(torch.randn(1, S, 1, D, generator=gen).bfloat16() for _ in range(3))
+
+
+def cpu_sample_dense(seconds: float, rows_per_sample: int = 512, qkv=None, first_block: int = 0,
+                     max_blocks: int | None = None):
+    """fp64 oracle on query-row blocks of one (batch, head) slice of the headline
+    workload (host cores); the slice is drawn before the clock starts.  Blocks are
+    taken with a stride of 13 blocks (coprime with the block count), so that a few
+    blocks already mix short and long causal rows."""
+    import numpy as np
+
+    from oracle import attention as A
+    cfg = __import__("synthetic").WORKLOADS[HEADLINE]
+    S, D = cfg["S_q"], cfg["D"]
+    q, k, v = qkv if qkv is not None else _cpu_slice()
     flops = 0.0
     n = 0
     t0 = time.perf_counter()
-    while True:
-        q = torch.randn(1, S, 1, D, generator=gen).bfloat16()
-        k = torch.randn(1, S, 1, D, generator=gen).bfloat16()
-        v = torch.randn(1, S, 1, D, generator=gen).bfloat16()
-        lo = (n * rows_per_sample) % S
+    while max_blocks is None or n < max_blocks:
+        n_blocks = (S + rows_per_sample - 1) // rows_per_sample
+        lo = (((first_block + n) * 13) % n_blocks) * rows_per_sample
         rows = np.arange(lo, min(S, lo + rows_per_sample))
         A.attention(q, k, v, 1 / math.sqrt(D), True, rows=rows)
         flops += 4.0 * D * float(np.sum(rows + 1))
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds:
+        if max_blocks is None and el >= seconds:
             break
-    return flops, el, n
+    return flops, time.perf_counter() - t0, n
 
 
 def cpu_baseline(seconds: float = 15.0):
@@ -396,15 +404,12 @@ def run_reference(args):
     if rank != 0:
         return 0
     W, K = args.warmup, args.steps
-    # each step: one block of 128 query rows against all its visible keys (bounded work)
-    for _ in range(min(W, 1)):
-        cpu_sample_dense(0.0, 128)
-    flops = 0.0
-    t0 = time.perf_counter()
-    for _ in range(K):
-        f, _, _ = cpu_sample_dense(0.0, 128)
-        flops += f
-    el = time.perf_counter() - t0
+    # each step: the next block of 128 query rows of one (batch, head) against all
+    # their visible keys (bounded work, blocks in the stride-13 order of
+    # cpu_sample_dense); the slice is drawn before the clock starts
+    qkv = _cpu_slice()
+    cpu_sample_dense(0.0, 128, qkv, 0, min(W, 1))
+    flops, el, _ = cpu_sample_dense(0.0, 128, qkv, 0, K)
     value = flops / el / 1e12
     line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": K,
             "warmup": W, "ms_per_step": round(el * 1e3 / K, 3), "higher_is_better": True, "scaling": "weak",
@@ -412,7 +417,8 @@ def run_reference(args):
             "config": {"workload": HEADLINE, "B": 8, "S": 4096, "h_q": 32, "h_kv": 32, "D": 256, "causal": True,
                        "sample_per_step": "128 query rows x visible keys of one (batch, head)"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{K} steps of 128 query rows of one (batch, head), fp64 NumPy"},
+                             "sample": f"{K} steps, each a block of 128 query rows of one (batch, head) "
+                                       f"against all their visible keys, fp64 NumPy"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
