@@ -243,6 +243,36 @@ def test_partial_causal_positions_and_identity(D):
     assert torch.all(torch.isneginf(m)) and torch.all(l == 0) and torch.all(o == 0)
 
 
+def test_partial_d256_persistent_many_units():
+    """Partials at head dim 256 run on the persistent grid: more two-tile units than
+    SMs, GQA, causal positions that leave some Q tiles fully visible, some partly and
+    some (the earliest rows) with no visible key at all, so that empty items and
+    identity rows sit between full ones in a CTA's sequence of units."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, S_q, S_kv, h_q, h_kv, D = 3, 520, 900, 48, 8, 256
+    assert B * h_q * (((S_q + 127) // 128 + 1) // 2) > sms
+    q, k, v = gen((B, S_q, h_q, D), (B, S_kv, h_kv, D), "bf16", seed=81)
+    scale = 1 / math.sqrt(D)
+    m = torch.empty(B, h_q, S_q, device="cuda")
+    l = torch.empty_like(m)
+    o = torch.empty(B, S_q, h_q, D, device="cuda")
+    # queries at positions 200..719 against keys [300, 800)
+    ra.attn_partial(q, k, v, m, l, o, scale=scale, causal=True, q_pos0=200, kv_begin=300, kv_end=800)
+    mr, lr, orr = A.partial(q.cpu(), k.cpu(), v.cpu(), scale, True, 200, 300, 800)
+    mg, lg = m.cpu().numpy(), l.cpu().numpy()
+    empty = np.isneginf(mr)
+    assert empty.any() and (~empty).any()
+    assert np.array_equal(np.isneginf(mg), empty)
+    assert np.all(lg[empty] == 0)
+    assert np.abs(mg[~empty] - mr[~empty]).max() <= 1e-3
+    assert np.abs(lg[~empty] / lr[~empty] - 1).max() <= 1e-3
+    full = ~np.swapaxes(empty, 1, 2)  # [B, S_q, h_q]
+    og = (o / l.clamp_min(1e-30).permute(0, 2, 1)[..., None]).cpu().numpy()
+    ref = orr / np.where(lr > 0, lr, 1.0).swapaxes(1, 2)[..., None]
+    close_o(torch.from_numpy(og[full]), ref[full], "partial D=256 persistent")
+    assert np.all(o.cpu().numpy()[~full] == 0)
+
+
 def test_merge_with_empty_partials_matches_full():
     B, S_, h, D = 2, 70, 3, 128
     q, k, v = gen((B, S_, h, D), (B, S_, h, D), "bf16", seed=5)
