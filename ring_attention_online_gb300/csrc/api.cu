@@ -357,6 +357,27 @@ attn_status_t attn_tile_walk(int q_lo, int q_hi, int kv_lo, int kv_hi, int block
     return ATTN_ERR_INVALID_ARG;
   TileWalk w;
   w.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, causal, num_chunks, block_n, window);
+  if (ring_walk_is_rotation(kv_lo, kv_hi, num_chunks, block_n)) {
+    // the paired kernel walks such rings as a rotated single-chunk walk; report
+    // that walk, with each tile's chunk and the chunk's own tail limit
+    TileWalk w1;
+    w1.init(q_lo, q_hi, kv_lo, kv_hi, q_pos0, kv_pos0, causal, 1, block_n, window);
+    LinearWalk lw;
+    lw.init(w1, ring_first_key(q_lo, kv_lo, kv_hi, q_pos0, kv_pos0, num_chunks), block_n);
+    const int len = kv_hi - kv_lo;
+    const int chunk_len = (len + num_chunks - 1) / num_chunks;
+    for (int i = 0; i < lw.n && i < max_tiles; ++i) {
+      int st, me;
+      lw.next(st, me, block_n);
+      const int c = (st - kv_lo) / chunk_len;
+      const long long chunk_hi = (long long)kv_lo + (long long)(c + 1) * chunk_len;
+      chunk[i] = c;
+      tile_start[i] = st;
+      mask_end[i] = (int)(me < chunk_hi ? me : chunk_hi);
+    }
+    *n_tiles = lw.n;
+    return ATTN_OK;
+  }
   const int total = w.count();
   int i = 0, c, st, me;
   while (i < max_tiles && w.next(c, st, me)) {

@@ -43,6 +43,8 @@
 // buffer and is the TMEM A operand of P.V.  Every wait is bounded.
 #pragma once
 
+#include <type_traits>
+
 #include "prefill_common.cuh"
 
 namespace attn {
@@ -155,17 +157,23 @@ __device__ __forceinline__ int pair_item_index(int r, int total) {
   return k < total ? (int)k : -2;  // -2: none this round, and none later
 }
 
-// kOneChunk: the launch walks a single chunk (no ring order); the literal lets
-// the compiler drop the ring-order walk state from every loop, which matters
-// at this kernel's register limit (jagged 472 -> 558 TFLOP/s, sliding window
-// 943 -> 1040)
-template <int D, bool kBf16, int kMode, bool kOneChunk>
+// kWalk: how an item's KV tiles are enumerated.  kWalkRing: the general
+// ring-order walk over num_chunks chunks.  kWalkOne: a single chunk; the
+// literal lets the compiler drop the ring-order walk state from every loop,
+// which matters at this kernel's register limit (jagged 472 -> 558 TFLOP/s,
+// sliding window 943 -> 1040).  kWalkRotated: a ring whose chunks are whole
+// tiles, walked as the single chunk rotated to the Q tile's own chunk (the
+// ring's tiles, masks and order; long ring 1233 -> 1311).
+enum PairWalk : int { kWalkRing = 0, kWalkOne = 1, kWalkRotated = 2 };
+
+template <int D, bool kBf16, int kMode, int kWalk>
 // 11 warps put three on three of the four SM sub-partitions (16K registers
 // each), so at most 168 registers per thread
 __global__ void __launch_bounds__(352, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = PairCfg<D>;
+  using Walk = std::conditional_t<kWalk == kWalkRotated, LinearWalk, TileWalk>;
   // dense / partial CTAs take one item; the item loops below then run once
   // (a loop the compiler cannot bound costs ~5% in the softmax code)
   constexpr bool kPersistent = kMode == kModeJagged || kMode == kModeWindow;
@@ -211,12 +219,28 @@ __global__ void __launch_bounds__(352, 1)
   // Per item, every role derives the same walk.  Sub-tile x takes part in the
   // tile starting at key `ks` iff it has rows and (causal) its last query
   // sees the tile's first key.
-  auto item_walk = [&](const PairItem& it, TileWalk& walk) -> int {
+  auto item_walk = [&](const PairItem& it, Walk& walk) -> int {
     const int u_lo = it.st0.q_lo;
     const int u_hi = it.st1.empty() ? it.st0.q_hi : max(it.st0.q_hi, it.st1.q_hi);
-    walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, kOneChunk ? 1 : p.num_chunks, C::BN,
+    if constexpr (kWalk == kWalkRotated) {
+      TileWalk w1;
+      w1.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, 1, C::BN,
               kMode == kModeWindow ? p.window : -1);
-    return walk.count();
+      walk.init(w1, ring_first_key(u_lo, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.num_chunks), C::BN);
+      return walk.n;
+    } else {
+      walk.init(u_lo, u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, kWalk == kWalkOne ? 1 : p.num_chunks,
+                C::BN, kMode == kModeWindow ? p.window : -1);
+      return walk.count();
+    }
+  };
+  auto walk_next = [&](Walk& walk, int& key, int& mask_end) {
+    if constexpr (kWalk == kWalkRotated) {
+      walk.next(key, mask_end, C::BN);
+    } else {
+      int ch;
+      walk.next(ch, key, mask_end);
+    }
   };
   auto active = [&](const PairItem& it, int x, int ks) -> bool {
     const SubTile t = x ? it.st1 : it.st0;
@@ -257,14 +281,14 @@ __global__ void __launch_bounds__(352, 1)
         const PairUnit un = pair_unit<kMode>(p, k);
         for (int ii = 0; ok && ii < un.n; ++ii) {
           const PairItem it = pair_item<kMode>(p, un.i0 + ii, un.h);
-          TileWalk walk;
+          Walk walk;
           const int n = item_walk(it, walk);
           if (n == 0) continue;
           const int hk = it.st0.h / p.group;
           // Q once the previous item's MMAs are done with the Q buffer, then
           // K/V in the MMA's first-use order: K(0), and per tile V(j), K(j+1)
-          TileWalk kw = walk, vw = walk;
-          int ch, s0, me;
+          Walk kw = walk, vw = walk;
+          int s0, me;
           if (q_loads > 0 && !pf_wait(&bar_qe, (uint32_t)((q_loads - 1) & 1), &abort_flag, 4)) {
             ok = false;
             break;
@@ -277,14 +301,14 @@ __global__ void __launch_bounds__(352, 1)
               tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, t.h, t.q_lo, it.b);
           }
           ++q_loads;
-          kw.next(ch, s0, me);
+          walk_next(kw, s0, me);
           ok = push(&mk, hk, s0, it.b);
           if (!ok) break;
           for (int j = 0; ok && j < n; ++j) {
-            vw.next(ch, s0, me);
+            walk_next(vw, s0, me);
             ok = push(&mv, hk, s0, it.b);
             if (ok && j + 1 < n) {
-              kw.next(ch, s0, me);
+              walk_next(kw, s0, me);
               ok = push(&mk, hk, s0, it.b);
             }
           }
@@ -331,7 +355,7 @@ __global__ void __launch_bounds__(352, 1)
         const PairUnit un = pair_unit<kMode>(p, k);
         for (int ii = 0; ok && ii < un.n; ++ii) {
           const PairItem it = pair_item<kMode>(p, un.i0 + ii, un.h);
-          TileWalk walk;
+          Walk walk;
           const int n = item_walk(it, walk);
           if (n == 0) continue;
           if (s_role) {
@@ -344,8 +368,8 @@ __global__ void __launch_bounds__(352, 1)
           }
           bool acc[2] = {false, false};  // O_x already holds this item's sum
           for (int j = 0; ok && j < n; ++j) {
-            int ch, kstart, me;
-            walk.next(ch, kstart, me);
+            int kstart, me;
+            walk_next(walk, kstart, me);
             const bool act[2] = {active(it, 0, kstart), active(it, 1, kstart)};
             const int slab = slab0 + 2 * j + (s_role ? 0 : 1);  // K(j) or V(j)
             ok = wait_slab(slab);
@@ -422,7 +446,7 @@ __global__ void __launch_bounds__(352, 1)
       const PairUnit un = pair_unit<kMode>(p, k);
       for (int ii = 0; ok && ii < un.n; ++ii) {
         const PairItem it = pair_item<kMode>(p, un.i0 + ii, un.h);
-        TileWalk walk;
+        Walk walk;
         const int n = item_walk(it, walk);
         const SubTile me_t = x ? it.st1 : it.st0;
         const int q_row = me_t.q_lo + row;
@@ -432,8 +456,8 @@ __global__ void __launch_bounds__(352, 1)
         float m_max = -CUDART_INF_F;  // true running max (partial mode)
         int cnt_item = 0;             // tiles of this item this sub-tile took part in
         for (int j = 0; j < n; ++j) {
-          int ch, kstart, mend;
-          walk.next(ch, kstart, mend);
+          int kstart, mend;
+          walk_next(walk, kstart, mend);
           if (!active(it, x, kstart)) continue;
           if (!pf_wait(&bar_s[x], (uint32_t)(cnt & 1), &abort_flag, 6)) {
             ok = false;
@@ -643,34 +667,39 @@ __global__ void __launch_bounds__(352, 1)
   }
 }
 
-template <int D, bool kBf16, int kMode, bool kOneChunk>
+template <int D, bool kBf16, int kMode, int kWalk>
 attn_status_t launch_pair_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
   using C = PairCfg<D>;
-  auto kern = prefill_pair_kernel<D, kBf16, kMode, kOneChunk>;
+  auto kern = prefill_pair_kernel<D, kBf16, kMode, kWalk>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Dense and window launches with one chunk, and every partial and jagged
-// launch (always one KV range), take the single-chunk instantiations.
+// Dense and window launches with one chunk take the single-chunk
+// instantiations, with ring chunks of whole tiles the rotated ones, otherwise
+// the general ring walk; every partial and jagged launch (always one KV range)
+// takes the single-chunk instantiation.
 template <int D, bool kBf16>
 attn_status_t launch_pair_typed(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                 const CUtensorMap& mv, int mode, dim3 grid, cudaStream_t s) {
   const bool one = p.num_chunks == 1;
+  const bool rotated = ring_walk_is_rotation(p.kv_lo, p.kv_hi, p.num_chunks, PairCfg<D>::BN);
   switch (mode) {
     case kModeDense:
-      return one ? launch_pair_variant<D, kBf16, kModeDense, true>(p, mq, mk, mv, grid, s)
-                 : launch_pair_variant<D, kBf16, kModeDense, false>(p, mq, mk, mv, grid, s);
+      return one       ? launch_pair_variant<D, kBf16, kModeDense, kWalkOne>(p, mq, mk, mv, grid, s)
+             : rotated ? launch_pair_variant<D, kBf16, kModeDense, kWalkRotated>(p, mq, mk, mv, grid, s)
+                       : launch_pair_variant<D, kBf16, kModeDense, kWalkRing>(p, mq, mk, mv, grid, s);
     case kModeWindow:
-      return one ? launch_pair_variant<D, kBf16, kModeWindow, true>(p, mq, mk, mv, grid, s)
-                 : launch_pair_variant<D, kBf16, kModeWindow, false>(p, mq, mk, mv, grid, s);
+      return one       ? launch_pair_variant<D, kBf16, kModeWindow, kWalkOne>(p, mq, mk, mv, grid, s)
+             : rotated ? launch_pair_variant<D, kBf16, kModeWindow, kWalkRotated>(p, mq, mk, mv, grid, s)
+                       : launch_pair_variant<D, kBf16, kModeWindow, kWalkRing>(p, mq, mk, mv, grid, s);
     case kModePartial:
-      return one ? launch_pair_variant<D, kBf16, kModePartial, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+      return one ? launch_pair_variant<D, kBf16, kModePartial, kWalkOne>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
     case kModeJagged:
-      return one ? launch_pair_variant<D, kBf16, kModeJagged, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+      return one ? launch_pair_variant<D, kBf16, kModeJagged, kWalkOne>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
   }
   return ATTN_ERR_INVALID_ARG;
 }

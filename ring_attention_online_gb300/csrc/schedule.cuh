@@ -115,4 +115,64 @@ struct TileWalk {
   }
 };
 
+// Whether the ring walk of num_chunks chunks over [kv_lo, kv_hi) is a rotation
+// of the single-chunk walk: it is when the chunk length is a multiple of
+// block_n.  Every chunk then starts on the range's block_n grid, so the ring
+// visits the single-chunk walk's tiles, with the same tail masks (no tile spans
+// two chunks), in the order: from the first tile of chunk c0 (the chunk of the
+// Q tile's first position) up, then from the first visible tile up to chunk c0.
+// Chunks past the causal limit hold no visible tile, and the chunks after c0
+// and the ones before it are each taken in ascending order, as in the ring.
+__host__ __device__ inline bool ring_walk_is_rotation(int kv_lo, int kv_hi, int num_chunks, int block_n) {
+  if (num_chunks <= 1) return false;
+  const int len = kv_hi - kv_lo;
+  const int chunk_len = len > 0 ? (len + num_chunks - 1) / num_chunks : 1;
+  return chunk_len % block_n == 0;
+}
+
+// First key of chunk c0 (the chunk that holds the Q tile's first position), as
+// TileWalk::init chooses it.
+__host__ __device__ inline int ring_first_key(int q_lo, int kv_lo, int kv_hi, int q_pos0, int kv_pos0,
+                                              int num_chunks) {
+  const int len = kv_hi - kv_lo;
+  const int chunk_len = len > 0 ? (len + num_chunks - 1) / num_chunks : 1;
+  const long long rel = (long long)q_pos0 + q_lo - ((long long)kv_pos0 + kv_lo);
+  long long c = rel <= 0 ? 0 : rel / chunk_len;
+  if (c > num_chunks - 1) c = num_chunks - 1;
+  const long long k = (long long)kv_lo + c * chunk_len;
+  return (int)(k < kv_hi ? k : kv_hi);
+}
+
+// The single-chunk walk's tiles [start, end), taken from the tile at key
+// `first` up and then from `start` up to it: with first = start it is the
+// single-chunk walk itself, with first = ring_first_key() the ring walk when
+// ring_walk_is_rotation() holds.  Three integers of state, for kernels whose
+// registers are scarce.
+struct LinearWalk {
+  int cur, start, end;
+  int n;  // tiles
+
+  __host__ __device__ void init(const TileWalk& one_chunk, int first, int block_n) {
+    if (one_chunk.t >= one_chunk.num_chunks) {  // nothing visible
+      start = end = cur = 0;
+      n = 0;
+      return;
+    }
+    start = one_chunk.cur;
+    end = one_chunk.end;
+    n = (end - start + block_n - 1) / block_n;
+    // first is on the start's block_n grid when it lies inside the range
+    cur = first > start && first < end ? first : start;
+  }
+
+  // Next tile: keys [key, key + block_n), the tail mask at mask_end.  Call it
+  // n times.
+  __host__ __device__ void next(int& key, int& mask_end, int block_n) {
+    key = cur;
+    mask_end = end;
+    cur += block_n;
+    if (cur >= end) cur = start;
+  }
+};
+
 }  // namespace attn

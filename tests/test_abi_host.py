@@ -148,6 +148,34 @@ def test_window_tile_walk_matches_oracle_bit_exact(lib, seed):
         assert [(c, st) for c, st, _ in got] == [(c, st) for c, st, _ in ref]
 
 
+@pytest.mark.parametrize("seed", range(60))
+def test_tile_walk_aligned_ring_is_the_rotated_linear_walk(lib, seed):
+    """Ring chunks whose length is a multiple of the 128-key tile: the library walks
+    them as its single-chunk walk rotated to start at the Q tile's own chunk.  The
+    tiles, their chunks and their order must equal the oracle's ring walk, with or
+    without causal masking, a sliding window and position offsets."""
+    rng = np.random.default_rng(1000 + seed)
+    C = int(rng.integers(2, 9))
+    L = 128 * int(rng.integers(1, 5))
+    S_kv = int(rng.integers((L - 1) * C + 1, L * C + 1))  # ceil(S_kv / C) == L
+    assert -(-S_kv // C) == L
+    S_q = S_kv if rng.random() < 0.6 else int(rng.integers(1, S_kv + 300))
+    causal = bool(rng.random() < 0.7)
+    window = int(rng.choice([0, 100, 128, 300, 1000])) if causal and rng.random() < 0.4 else -1
+    q_pos0 = int(rng.integers(-300, 300)) if rng.random() < 0.3 else 0
+    for lo, hi in S.dense_work_items(S_q, 128):
+        got = ra.attn_tile_walk(lo, hi, 0, S_kv, block_n=128, causal=causal, num_chunks=C, q_pos0=q_pos0,
+                                window=window)
+        ref = S.tile_walk(lo, hi, 0, S_kv, 128, causal, C, q_pos0, 0, None if window < 0 else window)
+        assert len(ref) > 0 or not causal or window >= 0 or q_pos0 < 0
+        assert [(c, st) for c, st, _ in got] == [(c, st) for c, st, _ in ref]
+        chunks, _ = S.ring_chunks(0, S_kv, C)
+        for (c, st, mend), (_, _, stop) in zip(got, ref):
+            assert mend <= chunks[c][1]
+            if mend < stop:
+                assert not S.pair_visible_in(lo, hi, mend, stop, causal, q_pos0, 0)
+
+
 def test_window_validation(lib):
     n = ctypes.c_int(0)
     assert lib.attn_tile_walk(0, 128, 0, 512, 128, 0, 1, 0, 0, 5, None, None, None, 0, ctypes.byref(n)) == 1  # window needs causal

@@ -84,6 +84,36 @@ def test_prefill_ring_gqa(C, causal):
     close_lse(lse, L)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S_,C,h_q,h_kv", [(1024, 4, 8, 2), (2048, 8, 4, 4), (1152, 3, 2, 2), (1100, 3, 6, 3)])
+def test_prefill_ring_chunks_of_whole_tiles(D, causal, S_, C, h_q, h_kv):
+    """Ring chunks whose length is a multiple of 128 keys (256, 384; 1100 / 3 -> 367 is
+    not, for contrast) run as the single-chunk walk rotated to each Q tile's own chunk:
+    head pairs and Q-tile pairs, 256-row items that straddle a chunk boundary (384-key
+    chunks), causal and not."""
+    B = 1
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=90 + C + D)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), causal)
+    close_o(o, O, f"ring of whole tiles S={S_} C={C} D={D}")
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("window", [0, 300, 700])
+def test_prefill_window_ring_chunks_of_whole_tiles(window):
+    B, S_, h_q, h_kv, D, C = 1, 2048, 8, 2, 128, 4
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=95 + window)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill_window(q, k, v, o, lse, window=window, num_chunks=C)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), True, window=window)
+    close_o(o, O, f"window ring of whole tiles w={window}")
+    close_lse(lse, L)
+
+
 # ---------------------------------------------------------------------- sliding window
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 129, 300, 5000])
