@@ -254,7 +254,11 @@ const char* attn_status_string(attn_status_t status);
  * attn_prefill_window's sliding window, window = -1 none.  Writes up to max_tiles entries
  * (chunk, tile_start, mask_end) in visiting order, where mask_end is the first
  * key index that the tile's tail mask excludes, and stores the full count in
- * *n_tiles.  Returns ATTN_ERR_INVALID_ARG on bad sizes or null pointers.
+ * *n_tiles.  When the chunk length is a multiple of block_n, the ring visits
+ * the tiles of the single-chunk walk in that walk's order rotated to the Q
+ * tile's own chunk, and the entries come from that rotated walk (the one the
+ * head-dim 64/128 kernels run), mask_end cut to the tile's chunk.  Returns
+ * ATTN_ERR_INVALID_ARG on bad sizes or null pointers.
  */
 attn_status_t attn_tile_walk(int q_lo, int q_hi, int kv_lo, int kv_hi, int block_n, int causal, int num_chunks,
                              int q_pos0, int kv_pos0, int window, int* chunk, int* tile_start, int* mask_end,
