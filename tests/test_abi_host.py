@@ -176,6 +176,22 @@ def test_tile_walk_aligned_ring_is_the_rotated_linear_walk(lib, seed):
                 assert not S.pair_visible_in(lo, hi, mend, stop, causal, q_pos0, 0)
 
 
+def test_tile_walk_aligned_ring_edges(lib):
+    """Rings of whole-tile chunks at their edges: a Q tile that sees nothing (queries
+    before every key), one whose own chunk is the last and shorter than the rest, one
+    that sees only its diagonal tile under a zero window, and a non-causal tile, which
+    visits every tile starting from its own chunk."""
+    assert ra.attn_tile_walk(0, 128, 0, 1024, causal=True, num_chunks=4, q_pos0=-500) == []
+    # 1017 keys in 8 chunks of 128: the last chunk holds 121 keys
+    w = ra.attn_tile_walk(896, 1017, 0, 1017, causal=True, num_chunks=8)
+    assert [(c, st) for c, st, _ in w] == [(7, 896)] + [(c, 128 * c) for c in range(7)]
+    assert w[0][2] == 1017  # the tail tile stops at the range's end
+    assert all(me == 128 * (c + 1) for c, _, me in w[1:])
+    assert ra.attn_tile_walk(512, 640, 0, 1024, causal=True, num_chunks=4, window=0) == [(2, 512, 640)]
+    w = ra.attn_tile_walk(300, 428, 0, 1024, causal=False, num_chunks=4)
+    assert [st for _, st, _ in w] == [256, 384, 512, 640, 768, 896, 0, 128]
+
+
 def test_window_validation(lib):
     n = ctypes.c_int(0)
     assert lib.attn_tile_walk(0, 128, 0, 512, 128, 0, 1, 0, 0, 5, None, None, None, 0, ctypes.byref(n)) == 1  # window needs causal
