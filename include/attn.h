@@ -201,7 +201,10 @@ size_t attn_decode_workspace_bytes(int B, int h_q, int D, int num_splits);
  * results as attn_decode_splitkv.  Returns ATTN_ERR_UNSUPPORTED when the partials,
  * attn_decode_workspace_bytes(B, h_q, D, num_splits), exceed the array.
  * The first call on a device looks up the array's device address (with that device
- * current); make that first call before any stream capture.  All calls share the
+ * current) and keeps it for the device's current context; a later context on the
+ * device (after a device reset) gets a fresh lookup on its first call.  Make the
+ * first call on a device, and the first after a reset, before any stream capture.
+ * All calls share the
  * array and it keeps the last call's contents (every entry a call reads is written
  * or zeroed by that call first); calls whose kernels overlap on the GPU race on it.
  */

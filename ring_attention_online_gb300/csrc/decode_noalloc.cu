@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "context_cache.h"
 
 namespace attn {
 namespace {
@@ -25,22 +26,64 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mutex;
+ContextAddressCache<kMaxDevices> g_scratch_addr;
 
-// Device address of the scratch array on the current device.  The host-side
-// symbol g_decode_scratch is only a stand-in, not a device address, so it is
-// looked up once per device with that device current and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Driver entry points for naming the current context (looked up once).
+bool ctx_functions(CtxGetCurrentFn* get_current, CtxGetIdFn* get_id) {
+  static CtxGetCurrentFn cur = nullptr;
+  static CtxGetIdFn id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  *get_current = cur;
+  *get_id = id;
+  return cur != nullptr && id != nullptr;
+}
+
+// Process-unique id of the calling thread's current context; false if there is none.
+bool current_context_id(unsigned long long* out) {
+  CtxGetCurrentFn get_current;
+  CtxGetIdFn get_id;
+  if (!ctx_functions(&get_current, &get_id)) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, out) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's current context.
+// The host-side symbol g_decode_scratch is only a stand-in, not a device
+// address.  The address is looked up with cudaGetSymbolAddress the first time
+// a device is used under a context and kept for that context; a new context
+// on the device (after a device reset) gets a fresh lookup, because the
+// module, and the array with it, may then sit at another address.
 attn_status_t scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  unsigned long long ctx_id = 0;
+  if (current_context_id(&ctx_id)) {
+    if (void* p = g_scratch_addr.get(dev, ctx_id)) {
+      *out = p;
+      return ATTN_OK;
+    }
   }
-  *out = g_scratch_addr[dev];
+  // the lookup also creates the device's primary context if the thread has none yet
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+  if (!current_context_id(&ctx_id)) return ATTN_ERR_CUDA;
+  g_scratch_addr.put(dev, ctx_id, p);
+  *out = p;
   return ATTN_OK;
 }
 

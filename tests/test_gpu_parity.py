@@ -71,34 +71,38 @@ def test_prefill_dense_ragged(D, dtype, causal, S_, h_q, h_kv):
     close_lse(lse, L)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("C", [2, 3, 8])
 @pytest.mark.parametrize("causal", [False, True])
-def test_prefill_ring_gqa(C, causal):
+def test_prefill_ring_gqa(C, causal, dtype):
+    """attn_prefill, general ring walk (1000 / C keys per chunk is not a whole number of
+    128-key tiles), GQA head pairs, both input types."""
     B, S_, h_q, h_kv, D = 1, 1000, 8, 2, 128
-    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=10 + C)
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), dtype, seed=10 + C)
     o = torch.empty_like(q)
     lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
     ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C)
     O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), causal)
-    close_o(o, O, f"ring C={C}")
+    close_o(o, O, f"attn_prefill ring C={C} {dtype}")
     close_lse(lse, L)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S_,C,h_q,h_kv", [(1024, 4, 8, 2), (2048, 8, 4, 4), (1152, 3, 2, 2), (1100, 3, 6, 3)])
-def test_prefill_ring_chunks_of_whole_tiles(D, causal, S_, C, h_q, h_kv):
+def test_prefill_ring_chunks_of_whole_tiles(D, causal, S_, C, h_q, h_kv, dtype):
     """Ring chunks whose length is a multiple of 128 keys (256, 384; 1100 / 3 -> 367 is
     not, for contrast) run as the single-chunk walk rotated to each Q tile's own chunk:
     head pairs and Q-tile pairs, 256-row items that straddle a chunk boundary (384-key
     chunks), causal and not."""
     B = 1
-    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=90 + C + D)
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), dtype, seed=90 + C + D)
     o = torch.empty_like(q)
     lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
     ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C)
     O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), causal)
-    close_o(o, O, f"ring of whole tiles S={S_} C={C} D={D}")
+    close_o(o, O, f"attn_prefill ring of whole tiles S={S_} C={C} D={D} {dtype}")
     close_lse(lse, L)
 
 
@@ -115,21 +119,22 @@ def test_prefill_window_ring_chunks_of_whole_tiles(window):
 
 
 # ---------------------------------------------------------------------- sliding window
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 129, 300, 5000])
 @pytest.mark.parametrize("h_q,h_kv", [(4, 2), (2, 2)])
-def test_prefill_window_parity(D, window, h_q, h_kv):
+def test_prefill_window_parity(D, window, h_q, h_kv, dtype):
     """Both kernels (paired for 64/128 with head pairs and Q-tile pairs, single-tile for
     256): the walk floor, the per-row lower mask and sub-tiles sitting out tiles below
     their window; window 5000 > S is plain causal."""
     B, S_ = 1, 650
-    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=window + D)
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), dtype, seed=window + D)
     o = torch.empty_like(q)
     lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
     scale = 1 / math.sqrt(D)
     ra.attn_prefill_window(q, k, v, o, lse, window=window, scale=scale)
     O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), scale, True, window=window)
-    close_o(o, O, f"window={window} D={D}")
+    close_o(o, O, f"attn_prefill_window window={window} D={D} {dtype}")
     close_lse(lse, L)
 
 
@@ -248,10 +253,12 @@ def test_tiny_config_partials_merge_and_ring():
     close_lse(lse2, L)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("D", [64, 128, 256])
-def test_partial_causal_positions_and_identity(D):
+def test_partial_causal_positions_and_identity(D, dtype):
+    """attn_partial with causal positions (q_pos0), a range that nothing sees and an empty range."""
     B, S_q, S_kv, h = 1, 160, 600, 2
-    q, k, v = gen((B, S_q, h, D), (B, S_kv, h, D), "bf16", seed=D)
+    q, k, v = gen((B, S_q, h, D), (B, S_kv, h, D), dtype, seed=D)
     scale = 1 / math.sqrt(D)
     qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
     # queries at positions 300..459 against keys [250, 520): partly visible, row by row
@@ -262,7 +269,7 @@ def test_partial_causal_positions_and_identity(D):
     mr, lr, orr = A.partial(qc, kc, vc, scale, True, 300, 250, 520)
     assert np.abs(m.cpu().numpy() - mr).max() <= 1e-3
     assert np.abs(l.cpu().numpy() / lr - 1).max() <= 1e-3
-    close_o(o / l.permute(0, 2, 1)[..., None], orr / np.swapaxes(lr, 1, 2)[..., None])
+    close_o(o / l.permute(0, 2, 1)[..., None], orr / np.swapaxes(lr, 1, 2)[..., None], f"attn_partial D={D} {dtype}")
     # queries at positions 0..159 against keys [400, 600): nothing visible -> identity
     ra.attn_partial(q, k, v, m, l, o, scale=scale, causal=True, q_pos0=0, kv_begin=400, kv_end=600)
     torch.cuda.synchronize()
@@ -303,9 +310,12 @@ def test_partial_d256_persistent_many_units():
     assert np.all(o.cpu().numpy()[~full] == 0)
 
 
-def test_merge_with_empty_partials_matches_full():
-    B, S_, h, D = 2, 70, 3, 128
-    q, k, v = gen((B, S_, h, D), (B, S_, h, D), "bf16", seed=5)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("D", [128, 256])
+def test_merge_with_empty_partials_matches_full(D, dtype):
+    """attn_partial over five causal ranges (two empty) then attn_merge into the input type."""
+    B, S_, h = 2, 70, 3
+    q, k, v = gen((B, S_, h, D), (B, S_, h, D), dtype, seed=5 + D)
     scale = 1 / math.sqrt(D)
     bounds = [(0, 10), (10, 10), (10, 69), (69, 70), (70, 70)]
     C = len(bounds)
@@ -318,15 +328,15 @@ def test_merge_with_empty_partials_matches_full():
     lse = torch.empty(B, h, S_, device="cuda")
     ra.attn_merge(m, l, o_un, out, lse)
     O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), scale, True)
-    close_o(out, O)
+    close_o(out, O, f"attn_merge D={D} {dtype}")
     close_lse(lse, L)
 
 
 # ---------------------------------------------------------------------- jagged
-def _jagged_case(lengths, H, D, seed, causal=True):
+def _jagged_case(lengths, H, D, seed, causal=True, dtype="bf16"):
     offs = syn.offsets_from_lengths(lengths)
     T = int(offs[-1])
-    q, k, v = syn.qkv((T, H, D), (T, H, D), "bf16", seed, "cuda")
+    q, k, v = syn.qkv((T, H, D), (T, H, D), dtype, seed, "cuda")
     o = torch.empty_like(q)
     lse = torch.empty(H, T, device="cuda")
     max_len = int(max(lengths)) if len(lengths) else 0
@@ -336,14 +346,16 @@ def _jagged_case(lengths, H, D, seed, causal=True):
     return q, k, v, o, lse, offs, ws
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [True, False])
-def test_jagged_parity_and_worklist(causal, D):
+def test_jagged_parity_and_worklist(causal, D, dtype):
+    """attn_jagged: zero-length, 1-token and 127/128/129-token sequences, both input types."""
     lengths = [0, 1, 5, 127, 128, 129, 300, 1024, 77, 0, 256, 640, 383, 384, 385]
     H = 2
-    q, k, v, o, lse, offs, ws = _jagged_case(lengths, H, D, seed=21, causal=causal)
+    q, k, v, o, lse, offs, ws = _jagged_case(lengths, H, D, seed=21, causal=causal, dtype=dtype)
     O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), causal)
-    close_o(o, O)
+    close_o(o, O, f"attn_jagged D={D} causal={causal} {dtype}")
     close_lse(lse, L)
     # worklist: the same items as the oracle's flattened worklist, bit for bit.  Head
     # dims 64/128 run two 128-row sub-tiles per CTA, so their Q tiles are 256 rows.
@@ -454,16 +466,31 @@ def test_jagged_random_lengths():
     (128, 8, 1, 100, 16),      # more splits than 64-key tiles: empty chunks
 ])
 def test_decode_parity_and_partials(D, h_q, h_kv, S_kv, splits):
+    _decode_case(D, h_q, h_kv, S_kv, splits, "bf16")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("G", [1, 8, 16])
+def test_decode_fp16_parity_and_partials(D, G):
+    """attn_decode_splitkv with fp16 inputs: the fused merge writes fp16 O; more splits
+    than 64-key tiles (700 keys in 40 chunks of 18) leave the last chunk empty, an
+    identity partial in the workspace."""
+    h_kv = 2
+    _decode_case(D, G * h_kv, h_kv, 700, 40, "fp16")
+
+
+def _decode_case(D, h_q, h_kv, S_kv, splits, dtype):
     B = 2
-    q, k, v = syn.qkv((B, h_q, D), (B, S_kv, h_kv, D), "bf16", S_kv + D, "cuda")
+    q, k, v = syn.qkv((B, h_q, D), (B, S_kv, h_kv, D), dtype, S_kv + D, "cuda")
     o = torch.empty_like(q)
     lse = torch.empty(B, h_q, device="cuda")
     ws = torch.empty(ra.attn_decode_workspace_bytes(B, h_q, D, splits), dtype=torch.uint8, device="cuda")
     scale = 1 / math.sqrt(D)
     ra.attn_decode_splitkv(q, k, v, o, ws, lse, num_splits=splits, scale=scale)
+    assert o.dtype == q.dtype
     qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
     O, L = A.decode(qc, kc, vc, scale, splits)
-    close_o(o, O)
+    close_o(o, O, f"attn_decode_splitkv D={D} G={h_q // h_kv} {dtype}")
     close_lse(lse, L)
     # the partial triplets in the documented workspace layout
     rows = splits * B * h_q
