@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libattn.so")
 SOURCES = ["api.cu", "prefill_d64.cu", "prefill_d128.cu", "prefill_d256.cu", "merge.cu", "worklist.cu", "decode.cu",
            "decode_noalloc.cu", "probe.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "schedule.cuh", "prefill_common.cuh", "prefill_kernel.cuh", "prefill_pair_kernel.cuh",
-           "merge.cuh", "context_cache.h"]
+           "merge.cuh", "context_cache.h", "prefill_cta2_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

@@ -51,9 +51,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Head dims 64 and 128 run two 128-row Q sub-tiles per CTA (query heads h, h+1 of
 // one KV group when the group size is even, else Q tiles 2t, 2t+1 of one head);
-// head dim 256 runs one Q tile per CTA (two of its O tiles do not fit in TMEM).
+// head dim 256 runs the same pairing over the two CTAs of a cluster (two of its
+// O tiles do not fit in one CTA's TMEM), each CTA one 128-row Q tile.  Either
+// way a jagged item is 256 rows.
 bool paired(int D) { return D <= 128; }
-int jagged_block(int D) { return paired(D) ? 2 * ATTN_BLOCK_M : ATTN_BLOCK_M; }
+int jagged_block(int) { return 2 * ATTN_BLOCK_M; }
+// Keys of a K tile each CTA of a head-dim-256 pair loads (the pair splits the
+// tile's keys between its CTAs).
+int k_box_rows(int D) { return paired(D) ? ATTN_BLOCK_N : ATTN_BLOCK_N / 2; }
 
 // Streaming multiprocessors of the current device (the persistent grid size).
 int sm_count() {
@@ -69,17 +74,25 @@ dim3 persistent_grid(long long items) {
   return dim3((unsigned)(g > 0 ? g : 1));
 }
 
+// Persistent grid of CTA pairs: one pair per two SMs, or fewer when there are
+// fewer units.
+dim3 persistent_pair_grid(long long units) {
+  const long long pairs = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+  const long long g = units < pairs ? units : pairs;
+  return dim3((unsigned)(2 * (g > 0 ? g : 1)));
+}
+
 // Fills the work-item decomposition of the paired kernel and its grid (one
 // item per CTA); the single-tile kernel runs one CTA per SM over units of two
 // Q tiles of one (batch, head).  False when the item count does not fit a
 // 32-bit item index.
 bool dense_grid(PrefillParams& p, int D, dim3* grid) {
   if (!paired(D)) {
-    // persistent over units of two Q tiles (see prefill_kernel.cuh)
-    const int n_qt = (p.S_q + ATTN_BLOCK_M - 1) / ATTN_BLOCK_M;
-    const long long units = (long long)((n_qt + 1) / 2) * p.h_q * p.B;
-    if (2 * ((units + sm_count() - 1) / sm_count()) > 0x7fffffffLL) return false;
-    *grid = persistent_grid(units);
+    // CTA pairs, persistent over units of up to two pair items (see prefill_cta2_kernel.cuh)
+    const long long units = cta2_units(p.B, p.S_q, p.h_q, p.pair_heads);
+    const long long pairs = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+    if (2 * ((units + pairs - 1) / pairs) > 0x7fffffffLL) return false;
+    *grid = persistent_pair_grid(units);
     return true;
   }
   const int rows = p.pair_heads ? ATTN_BLOCK_M : 2 * ATTN_BLOCK_M;
@@ -149,7 +162,7 @@ attn_status_t prefill_impl(const void* q, const void* k, const void* v, void* o,
   p.pair_heads = (p.group % 2) == 0;
   p.window = window;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
+  if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, k_box_rows(D)) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
   dim3 grid;
@@ -208,7 +221,7 @@ attn_status_t attn_partial(const void* q, const void* k, const void* v, float* m
   p.scale_log2 = scale * kLog2e;
   p.pair_heads = (p.group % 2) == 0;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N) ||
+  if (!make_map(&mq, q, bf16, D, h_q, S_q, B, ATTN_BLOCK_M) || !make_map(&mk, k, bf16, D, h_kv, S_kv, B, k_box_rows(D)) ||
       !make_map(&mv, v, bf16, D, h_kv, S_kv, B, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
   dim3 grid;
@@ -274,11 +287,12 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
   p.work_units = reinterpret_cast<const int2*>(wl + 4 + 4 * max_items);
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, bf16, D, H, total_tokens, 1, ATTN_BLOCK_M) ||
-      !make_map(&mk, k, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N) ||
+      !make_map(&mk, k, bf16, D, H, total_tokens, 1, k_box_rows(D)) ||
       !make_map(&mv, v, bf16, D, H, total_tokens, 1, ATTN_BLOCK_N))
     return ATTN_ERR_CUDA;
-  // paired kernel: persistent over (sequence, head) units; otherwise one CTA per (item, head)
-  const dim3 grid = paired(D) ? persistent_grid((long long)num_seqs * H) : dim3((unsigned)max_items, H, 1);
+  // paired kernel: persistent over (sequence, head) units; CTA pairs: one pair per (item, head)
+  if (!paired(D) && 2 * max_items > 0x7fffffffULL) return ATTN_ERR_UNSUPPORTED;
+  const dim3 grid = paired(D) ? persistent_grid((long long)num_seqs * H) : dim3((unsigned)(2 * max_items), H, 1);
   return launch_prefill(p, mq, mk, mv, kModeJagged, bf16, D, grid, s);
 }
 

@@ -39,7 +39,6 @@ static __device__ __noinline__ bool pf_wait_slow(uint32_t a, uint32_t parity, vo
                                                  uint32_t site) {
   return pf_spin(a, parity, abort, site);
 }
-
 // Bounded wait used by every role; also gives up once another CTA of any
 // launch has reported a timeout, so a broken pipeline ends quickly.  The
 // barrier is polled first: the clock and the device-wide status word (a
@@ -70,15 +69,16 @@ __device__ __forceinline__ bool pf_wait_outlined(uint64_t* bar, uint32_t parity,
 }
 
 // Wait used only while tearing down after an abort: ignores the abort flag.
-__device__ __forceinline__ void pf_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool pf_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(a, parity)) {
     if (global_timer_ns() - t0 > kWaitTimeoutNs) {
       atomicOr(&g_prefill_status, kStatusTimeout | (0x80u << kStatusSiteShift));
-      return;
+      return false;
     }
   }
+  return true;
 }
 
 inline unsigned int prefill_take_status_impl(cudaStream_t s) {

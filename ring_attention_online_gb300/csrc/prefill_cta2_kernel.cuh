@@ -1,0 +1,757 @@
+// Blockwise online-softmax attention forward for head dimension 256 on CTA
+// pairs: tcgen05 with cta_group::2, 256 query rows per pair sharing every K/V
+// tile.
+//
+// What it computes, by source (the same as the paired and single-tile kernels):
+//  * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel: per KV block,
+//    scores = Q.K^T, m = rowmax, exp(scores - m), l = rowsum, O = exp . V,
+//    merged into the running (m, l, O) with m_new = max(m, m_step) and the
+//    factors exp(m - m_new), exp(m_step - m_new); O / l at the end.  The blocks
+//    are 128-key tiles of a ring-order walk over the chunks.
+//  * "[pallas] Support dependent Tile.end bounds in Pallas": the walk ends at
+//    min(kv_end, tile_q.end); only the diagonal and tail tiles are masked.
+//  * The module docstring of the prefill page, P6c: the query rows of one unit
+//    are tiled over its processing elements, which share the unit's K/V.  Here
+//    the unit is the two SMs of a TPC.
+//
+// Why pairs.  A single CTA computing a 128 x 128 x 256 score tile and its P.V
+// moves 320 KB through its shared memory per KV tile (the S MMAs read 128 KB
+// of Q and K, the P.V MMAs 64 KB of V, the copies write 128 KB) against 2048
+// tensor cycles, more than the shared memory delivers in that time (128 B per
+// cycle).  In a pair, one MMA instruction covers M = 256 rows: each CTA
+// supplies its own 128 rows of Q (and of P, from its TMEM) and half of the B
+// operand (64 keys of K, 64 columns of each 128-column V slab), and each CTA's
+// TMEM receives its own rows of S and O.  Per CTA and KV tile the shared
+// memory then moves 192 KB: the S MMAs read 96 KB, the P.V MMAs 32 KB, the
+// copies write 64 KB.
+//
+// Work: a pair item is 256 query rows that walk one KV sequence: two
+// consecutive 128-row Q tiles of one (batch, head), the even CTA of the pair
+// (rank 0) taking the first, walking the later tile's KV tiles (the earlier
+// tile's rows see every key of all but the last tile, whose keys they mask);
+// with GQA and an even group size, the same Q tile of two query heads of one
+// KV group (identical walks).  Dense, partial and window launches are
+// persistent: cluster c takes units c, c + clusters, ..., a unit being two
+// items of one (batch, head or head pair) whose causal walks add up to the
+// same length (items x and n - 1 - x), the longer first.  A jagged cluster
+// takes one worklist item of 256 rows.
+//
+// CTA layout (352 threads; both CTAs of the pair run the same roles except
+// where noted):
+//   warp 0      TMA producer: this CTA's Q tile, then its halves of the K and V
+//               slabs through a K ring and a V ring of shared-memory stages,
+//               each copy completing on this CTA's own barrier.
+//   warp 1      rank 0: TMEM owner and S issuer, S(j) = Q.K_j^T for the pair.
+//               rank 1: TMEM owner and relay: forwards each completed copy of
+//               its CTA (Q and every slab) to rank 0 by a remote mbarrier
+//               arrival, so the issuers know both halves have landed.
+//   warp 10     rank 0: P.V issuer.  rank 1: idle.
+//   warps 2..9  softmax + epilogue of this CTA's 128 rows, two warps per row (a
+//               half of the tile's keys and of O's columns each), exactly as in
+//               the single-tile kernel; their "S read" and "P written" signals
+//               go to rank 0's barriers (one arrival per warp).
+// Every MMA commit is multicast to both CTAs' barriers.  Every wait is bounded:
+// a timeout sets the library's device status, the CTA skips its remaining
+// work, drains its own copies and (rank 0) its MMAs, and both CTAs meet at a
+// bounded exit handshake before freeing TMEM, so neither leaves while the
+// other may still signal it.
+#pragma once
+
+#include <math_constants.h>
+
+#include "prefill_common.cuh"
+
+namespace attn {
+
+struct Cta2Cfg {
+  static constexpr int D = 256;
+  static constexpr int BM = 128;                // query rows per CTA (256 per pair)
+  static constexpr int BN = 128;                // keys per KV tile
+  static constexpr int SC = 128;                // columns of D per K or V slab
+  static constexpr int NH = D / SC;             // slabs per K or V tile
+  static constexpr int KH = BN / 2;             // keys of a K slab each CTA holds
+  static constexpr int VH = SC / 2;             // columns of a V slab each CTA holds
+  static constexpr int Q_BLOCK = 128 * 128;     // Q: 128 rows x 64 columns (128 B, swizzled)
+  static constexpr int K_BLOCK = KH * 128;      // K half: 64 keys x 64 columns
+  static constexpr int Q_BYTES = BM * D * 2;    // 64 KB
+  static constexpr int STAGE_BYTES = 16384;     // K half slab 64 x 128, V half slab 128 x 64
+  static constexpr int RING = 4;                // stages per ring: two tiles of K, two of V
+  static constexpr int NST = 2 * RING;
+  // + 1 KB alignment slack, + one stage of slack after the last stage: an MMA
+  // operand span never reaches past the CTA's allocation
+  static constexpr int SMEM_BYTES = Q_BYTES + NST * STAGE_BYTES + 1024 + STAGE_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM (each CTA, its own 128 rows): S(j) in [0, 128); P(j) (16-bit) in
+  // [P_COL + 64 (j % 2), +64); O in [O_COL, O_COL + 256)
+  static constexpr uint32_t P_COL = 128;
+  static constexpr uint32_t O_COL = 256;
+  static constexpr int THREADS = 352;
+  static constexpr uint16_t kBoth = 3;          // multicast mask of a commit: both CTAs
+  static constexpr uint32_t kSignals = 16;      // arrivals per phase: the pair's 16 softmax warps
+  static_assert(KH * SC * 2 == STAGE_BYTES && BN * VH * 2 == STAGE_BYTES, "stage size");
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES + 8 * 1024 <= 227 * 1024, "shared memory budget (static part ~7 KB)");
+};
+
+template <bool kBf16, int kMode, bool kOneChunk>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
+    prefill_cta2_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                        const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
+  using C = Cta2Cfg;
+  constexpr int D = C::D;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_pq, bar_qe, bar_fin, bar_exit;
+  __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2] (both CTAs)
+  __shared__ uint64_t bar_full[C::NST], bar_pfull[C::NST], bar_empty[C::NST];
+  __shared__ uint64_t bar_s[2], bar_p[2];
+  __shared__ uint64_t bar_sfree[2];  // the pair's softmax warps have read S(j) out of TMEM (j % 2)
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t abort_flag;
+  __shared__ float xch_max[2][2][128];                   // [tile parity][column half][row]
+  __shared__ float xch_l[2][2][128], xch_lr[2][2][128];  // [item parity][column half][row]
+  __shared__ uint64_t bar_x[2][4];                       // pair-of-warps exchange: [tile parity][lane quarter]
+  __shared__ uint64_t bar_xe[4];                         // end-of-row exchange per lane quarter
+
+  const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs of the pair
+  const int cl = (int)(blockIdx.x >> 1);
+  const int n_cl = (int)(gridDim.x >> 1);
+
+  // ------------------------------------------------------------ work items
+  struct Item {
+    int b, h;      // this CTA's batch and query head
+    int q_lo, q_hi;  // this CTA's rows (none when q_hi <= q_lo)
+    int u_lo, u_hi;  // the pair's rows: the walk's query range
+    int kv_lo, kv_hi, q_pos0, kv_pos0;
+    bool valid;
+  };
+  const int n_qt = (p.S_q + C::BM - 1) / C::BM;
+  const int n_it = p.pair_heads ? n_qt : (n_qt + 1) / 2;  // items per (batch, head pair or head)
+  const int n_ux = (n_it + 1) / 2;                        // units per (batch, head pair or head)
+  const int n_y = p.pair_heads ? p.h_q / 2 : p.h_q;
+  int n_my = 1;  // item slots of this pair
+  if constexpr (kMode == kModeJagged) {
+    if (cl >= *p.work_count) return;  // both CTAs of the pair read the same count
+  } else {
+    const long long units = (long long)n_ux * n_y * p.B;
+    n_my = 2 * (int)((units - (long long)cl + n_cl - 1) / n_cl);
+  }
+  auto get_item = [&](int i) -> Item {
+    Item it;
+    it.valid = true;
+    if constexpr (kMode == kModeJagged) {
+      (void)i;
+      const int4 w = p.work_items[cl];  // 256 rows of one sequence
+      it.b = 0;
+      it.h = blockIdx.y;
+      it.u_lo = w.z;
+      it.u_hi = w.z + w.w;
+      it.kv_lo = w.x;
+      it.kv_hi = w.x + w.y;  // seq_offsets[seq_idx + 1]
+      it.q_pos0 = 0;
+      it.kv_pos0 = 0;
+      it.q_lo = it.u_lo + C::BM * (int)rank;
+      it.q_hi = min(it.q_lo + C::BM, it.u_hi);
+    } else {
+      const long long u = (long long)cl + (long long)(i >> 1) * n_cl;
+      const int x = (int)(u % n_ux);
+      const long long yb = u / n_ux;
+      int xi;
+      if (p.causal) {
+        const int x_first = n_it - 1 - x;
+        xi = (i & 1) ? x : x_first;
+        it.valid = !(i & 1) || x < x_first;
+      } else {
+        xi = 2 * x + (i & 1);
+        it.valid = xi < n_it;
+      }
+      it.b = (int)(yb / n_y);
+      const int y = (int)(yb % n_y);
+      if (p.pair_heads) {
+        it.h = 2 * y + (int)rank;
+        it.u_lo = xi * C::BM;
+        it.u_hi = min(it.u_lo + C::BM, p.S_q);
+        it.q_lo = it.u_lo;
+        it.q_hi = it.u_hi;
+      } else {
+        it.h = y;
+        it.u_lo = xi * 2 * C::BM;
+        it.u_hi = min(it.u_lo + 2 * C::BM, p.S_q);
+        it.q_lo = it.u_lo + C::BM * (int)rank;
+        it.q_hi = min(it.q_lo + C::BM, it.u_hi);
+      }
+      it.kv_lo = p.kv_lo;
+      it.kv_hi = p.kv_hi;
+      it.q_pos0 = p.q_pos0;
+      it.kv_pos0 = p.kv_pos0;
+    }
+    return it;
+  };
+  // the pair's walk: every role of both CTAs derives the same one
+  auto item_walk = [&](const Item& it, TileWalk& w) -> int {
+    w.init(it.u_lo, it.u_hi, it.kv_lo, it.kv_hi, it.q_pos0, it.kv_pos0, p.causal, kOneChunk ? 1 : p.num_chunks, C::BN,
+           kMode == kModeWindow ? p.window : -1);
+    return w.count();
+  };
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::Q_BYTES;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_pq, 1);
+    mbar_init(&bar_qe, 1);
+    mbar_init(&bar_o[0], 1);
+    mbar_init(&bar_o[1], 1);
+    mbar_init(&bar_fin, 2);  // one commit per MMA issuer, multicast to both CTAs
+    mbar_init(&bar_exit, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_pfull[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_sfree[i], C::kSignals);
+      mbar_init(&bar_p[i], C::kSignals);
+      for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 64);
+    }
+    for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_xe[q4], 64);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_cta2(&tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_cta2();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  // both CTAs' barriers are initialised before either signals the other's
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ========================================================== TMA producer (both CTAs)
+    if (lane == 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      int filled[2] = {0, 0};  // slabs issued into the K ring and the V ring
+      int q_loads = 0;
+      bool ok = true;
+      int hk = 0, bb = 0;
+      // fill f of a ring goes to its stage f % RING, once the pair's MMAs have
+      // released fill f - RING of that stage (the commit reaches both CTAs)
+      auto push_tile = [&](int ring, int kstart) -> bool {
+        int& fills = filled[ring];
+        for (int hs = 0; hs < C::NH; ++hs, ++fills) {
+          const int stage = ring * C::RING + fills % C::RING;
+          const uint32_t phase = (uint32_t)((fills / C::RING) & 1);
+          if (!pf_wait_outlined(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
+          uint8_t* dst = sKV + stage * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&bar_full[stage], C::STAGE_BYTES);
+          if (ring == 0) {
+            // K: this CTA's 64 keys of the tile, the slab's 128 columns
+            for (int blk = 0; blk < C::SC / 64; ++blk)
+              tma_load_4d(dst + blk * C::K_BLOCK, &mk, &bar_full[stage], hs * C::SC + blk * 64, hk,
+                          kstart + C::KH * (int)rank, bb);
+          } else {
+            // V: the tile's 128 keys, this CTA's 64 columns of the slab
+            tma_load_4d(dst, &mv, &bar_full[stage], hs * C::SC + C::VH * (int)rank, hk, kstart, bb);
+          }
+        }
+        return true;
+      };
+      for (int i = 0; ok && i < n_my; ++i) {
+        const Item it = get_item(i);
+        if (!it.valid) continue;
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        hk = it.h / p.group;
+        bb = it.b;
+        // the Q buffer is free once the previous item's S MMAs are done
+        if (q_loads > 0 && !pf_wait_outlined(&bar_qe, (uint32_t)((q_loads - 1) & 1), &abort_flag, 13)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(sQ + blk * C::Q_BLOCK, &mq, &bar_q, blk * 64, it.h, it.q_lo, it.b);
+        ++q_loads;
+        TileWalk kw = walk, vw = walk;
+        int ch, st, me;
+        kw.next(ch, st, me);
+        ok = push_tile(0, st);
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n) {
+            kw.next(ch, st, me);
+            ok = push_tile(0, st);
+            if (!ok) break;
+          }
+          vw.next(ch, st, me);
+          ok = push_tile(1, st);
+        }
+      }
+      if (abort_flag) {
+        // this CTA's copies may still be landing in its shared memory: wait for them
+        if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
+        for (int ring = 0; ring < 2; ++ring) {
+          const int outstanding = filled[ring] < C::RING ? filled[ring] : C::RING;
+          for (int i = 0; i < outstanding; ++i) {
+            const int pos = filled[ring] - 1 - i;
+            pf_drain(&bar_full[ring * C::RING + pos % C::RING], (uint32_t)((pos / C::RING) & 1));
+          }
+        }
+      }
+    }
+  } else if (warp == 1 && rank != 0) {
+    // ========================================================== relay (rank 1)
+    // Forwards, in the producer's order, each completed copy of this CTA to the
+    // matching barrier of rank 0 (bar_pq for Q, bar_pfull for a slab).
+    if (lane == 0) {
+      const uint32_t pq_remote = mapa_shared(&bar_pq, 0);
+      int filled[2] = {0, 0};
+      int q_loads = 0;
+      bool ok = true;
+      auto relay_tile = [&](int ring) -> bool {
+        for (int hs = 0; hs < C::NH; ++hs) {
+          const int f = filled[ring]++;
+          const int stage = ring * C::RING + f % C::RING;
+          if (!pf_wait_outlined(&bar_full[stage], (uint32_t)((f / C::RING) & 1), &abort_flag, 14)) return false;
+          mbar_arrive_remote(mapa_shared(&bar_pfull[stage], 0));
+        }
+        return true;
+      };
+      for (int i = 0; ok && i < n_my; ++i) {
+        const Item it = get_item(i);
+        if (!it.valid) continue;
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        ok = pf_wait_outlined(&bar_q, (uint32_t)(q_loads & 1), &abort_flag, 15);
+        if (!ok) break;
+        mbar_arrive_remote(pq_remote);
+        ++q_loads;
+        ok = relay_tile(0);
+        for (int j = 0; ok && j < n; ++j) {
+          if (j + 1 < n) {
+            ok = relay_tile(0);
+            if (!ok) break;
+          }
+          ok = relay_tile(1);
+        }
+      }
+      // rank 0's MMAs read this CTA's shared memory and write its TMEM: they
+      // finish before this CTA tears down (the final commits reach both CTAs)
+      pf_drain(&bar_fin, 0);
+    }
+  } else if (warp == 1 || warp == 10) {
+    // ========================================================== MMA issuers (rank 0)
+    // Warp 1 issues S(j), warp 10 PV(j), for the whole pair.  Each only waits
+    // on work of other roles (a wait stalls until the thread's own issued
+    // tcgen05 work has drained): the S issuer on K slabs and on the softmax
+    // having read S(j-1); the PV issuer on P(j) and V slabs.  A slab is ready
+    // when both CTAs' halves have landed: this CTA's copy completes bar_full,
+    // rank 1's is relayed to bar_pfull.
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t kIdescS = idesc_f16_f32acc(256, C::BN, kBf16, false);
+      constexpr uint32_t kIdescPV = idesc_f16_f32acc(256, C::SC, kBf16, true);
+      const uint32_t skv = smem_u32(sKV);
+      auto wait_slab = [&](int ring, int f, uint32_t site) -> bool {
+        const int stage = ring * C::RING + f % C::RING;
+        const uint32_t ph = (uint32_t)((f / C::RING) & 1);
+        if (!pf_wait_outlined(&bar_full[stage], ph, &abort_flag, site)) return false;
+        if (!pf_wait_outlined(&bar_pfull[stage], ph, &abort_flag, site)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      bool ok = true;
+      int g = 0;          // S (or PV) groups issued so far, all items: barrier phases
+      int slab_base = 0;  // slabs of this issuer's ring taken by the earlier items
+      int q_used = 0;     // Q tiles consumed (S issuer)
+      for (int i = 0; ok && i < n_my; ++i) {
+        const Item it = get_item(i);
+        if (!it.valid) continue;
+        TileWalk walk;
+        const int n = item_walk(it, walk);
+        if (n == 0) continue;
+        if (warp == 1) {
+          const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+          ok = pf_wait_outlined(&bar_q, (uint32_t)(q_used & 1), &abort_flag, 5) &&
+               pf_wait_outlined(&bar_pq, (uint32_t)(q_used & 1), &abort_flag, 5);
+          tc_fence_after_sync();
+          ++q_used;
+          for (int j = 0; ok && j < n; ++j, ++g) {
+            if (g >= 1) {
+              // the one S buffer is free once both CTAs' softmax warps have read S(j-1)
+              ok = pf_wait_outlined(&bar_sfree[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), &abort_flag, 11);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
+            for (int hs = 0; hs < C::NH; ++hs) {
+              const int sl = slab_base + j * C::NH + hs;
+              ok = wait_slab(0, sl, 2);
+              if (!ok) break;
+              const uint64_t kdesc = smem_desc_sw128(skv + (sl % C::RING) * C::STAGE_BYTES, 16, 1024);
+#pragma unroll
+              for (int ks = 0; ks < C::SC / 16; ++ks) {
+                // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle row,
+                // the next 64-column block every four steps
+                const uint32_t qoff = (hs * (C::SC / 64) + ks / 4) * C::Q_BLOCK + (ks % 4) * 32;
+                const uint32_t koff = (ks / 4) * C::K_BLOCK + (ks % 4) * 32;
+                mma_ss_cta2(tmem, desc_advance(qdesc, qoff), desc_advance(kdesc, koff), kIdescS, (hs | ks) != 0);
+              }
+              mma_commit_cta2(&bar_empty[sl % C::RING], C::kBoth);
+            }
+            if (!ok) break;
+            mma_commit_cta2(&bar_s[g & 1], C::kBoth);
+          }
+          // the item's S MMAs, the last readers of its Q, release both Q buffers
+          if (ok) mma_commit_cta2(&bar_qe, C::kBoth);
+        } else {
+          for (int j = 0; ok && j < n; ++j, ++g) {
+            ok = pf_wait_outlined(&bar_p[g & 1], (uint32_t)((g >> 1) & 1), &abort_flag, 3);
+            if (!ok) break;
+            tc_fence_after_sync();  // P of both CTAs in TMEM
+            const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((g & 1) * 64);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;  // the item's first PV starts O afresh
+            for (int hs = 0; hs < C::NH; ++hs) {
+              const int sl = slab_base + j * C::NH + hs;
+              ok = wait_slab(1, sl, 4);
+              if (!ok) break;
+              const int stage = C::RING + sl % C::RING;
+              const uint64_t vdesc = smem_desc_sw128(skv + stage * C::STAGE_BYTES, 16384, 1024);
+              // 16 keys of V per MMA (16 rows of 128 bytes)
+#pragma unroll
+              for (int ks = 0; ks < C::BN / 16; ++ks)
+                mma_ts_cta2(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                            ks > 0 ? 1u : acc0);
+              mma_commit_cta2(&bar_empty[stage], C::kBoth);
+            }
+            if (!ok) break;
+            mma_commit_cta2(&bar_o[g & 1], C::kBoth);
+          }
+        }
+        slab_base += n * C::NH;
+      }
+      // every MMA either issuer issued must finish before TMEM is released (both CTAs)
+      mma_commit_cta2(&bar_fin, C::kBoth);
+      pf_drain(&bar_fin, 0);
+    }
+  } else if (warp >= 2 && warp <= 9) {
+    // ========================================================== softmax + epilogue (both CTAs)
+    // Two warps share each TMEM lane quarter: warp (2 + wq) and (6 + wq) take the
+    // two column halves of every row (keys [64 half, 64 half + 64) of a tile, O
+    // columns [half D/2, half D/2 + D/2)).  The two exchange row maxima once per
+    // tile through shared memory, so both halves take identical decisions.
+    const int sw = warp - 2;  // 0..7
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = sw >> 2;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    constexpr int HD = D / 2;  // O columns per half
+    const float c = p.scale_log2;  // > 0
+    const uint32_t sfree_remote[2] = {mapa_shared(&bar_sfree[0], 0), mapa_shared(&bar_sfree[1], 0)};
+    const uint32_t p_remote[2] = {mapa_shared(&bar_p[0], 0), mapa_shared(&bar_p[1], 0)};
+    // one arrival per warp on rank 0's barrier: local there, remote from rank 1
+    auto signal = [&](uint64_t* local, uint32_t remote) {
+      if (rank == 0)
+        mbar_arrive(local);
+      else
+        mbar_arrive_remote(remote);
+    };
+    bool ok = true;
+    int gj = 0;    // tiles so far, all items: the phases of the per-tile barriers
+    int n_ep = 0;  // epilogues so far
+    for (int i = 0; ok && i < n_my; ++i) {
+      const Item it = get_item(i);
+      if (!it.valid) continue;
+      TileWalk sw_walk;
+      const int n = item_walk(it, sw_walk);
+      const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
+      const int q_row = q_lo + row;
+      float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
+      float l_run = 0.f;             // this half's sum of exp2(x - m_run) in fp32: l and LSE
+      float lr_run = 0.f;            // this half's sum of the rounded P the MMA multiplies V by
+      float m_max = -CUDART_INF_F;   // true running max (partial mode)
+      for (int j = 0; j < n; ++j, ++gj) {
+        int ch, kstart, mend;
+        sw_walk.next(ch, kstart, mend);
+        const int buf = gj & 1;
+        if (!pf_wait_outlined(&bar_s[buf], (uint32_t)((gj >> 1) & 1), &abort_flag, 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(lane_addr + half * 64, r0);
+        tmem_ld32(lane_addr + half * 64 + 32, r1);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        // S(j) is in registers: the S issuer may overwrite the buffer with S(j+1)
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) signal(&bar_sfree[buf], sfree_remote[buf]);
+
+        // mask the diagonal / tail tile (key kstart + i is visible iff i < lim)
+        // and, under a sliding window, the tiles at its lower edge (iff i >= flo);
+        // the pair's walk may hold tiles that none of this CTA's rows sees
+        constexpr bool win = kMode == kModeWindow;
+        const bool need_mask =
+            (kstart + C::BN > mend) ||
+            (p.causal && ((long long)kv_pos0 + kstart + C::BN - 1 > (long long)q_pos0 + q_lo)) ||
+            (win && (long long)kv_pos0 + kstart < (long long)q_pos0 + q_hi - 1 - p.window);
+        if (need_mask) {
+          long long lim = (long long)mend - kstart;
+          long long flo = 0;
+          if (p.causal) {
+            const long long lc = (long long)q_pos0 + q_row - kv_pos0 - kstart + 1;
+            lim = lc < lim ? lc : lim;
+            if (win) flo = lc - 1 - p.window;
+          }
+          const long long lh = lim - half * 64, fh = flo - half * 64;  // limits within this half
+          const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (k >= lh || k < fh) r0[k] = ninf;
+            if (k + 32 >= lh || k + 32 < fh) r1[k] = ninf;
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mx8[k] = fmax3(__uint_as_float(r0[k]), __uint_as_float(r0[k + 8]), __uint_as_float(r0[k + 16]));
+          mx8[k] = fmax3(mx8[k], __uint_as_float(r0[k + 24]), __uint_as_float(r1[k]));
+          mx8[k] = fmax3(mx8[k], __uint_as_float(r1[k + 8]), __uint_as_float(r1[k + 16]));
+          mx8[k] = fmaxf(mx8[k], __uint_as_float(r1[k + 24]));
+        }
+        float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        // both halves of the row see each other's max
+        xch_max[buf][half][row] = mx;
+        mbar_arrive(&bar_x[buf][wq]);
+        if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((gj >> 1) & 1), &abort_flag, 9)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, xch_max[buf][half ^ 1][row]);
+        const float m_tile = mx * c;  // -inf when the whole row is masked
+        if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool raise = (m_new - m_run) > 8.0f;  // false when both are -inf
+        float alpha = 1.f;
+        if (raise) {
+          alpha = fast_exp2(m_run - m_new);  // 0 on the first visible tile
+          m_run = m_new;
+          l_run *= alpha;
+          lr_run *= alpha;
+        }
+        // P goes to P buffer gj % 2, which the PV two tiles back read; that PV is
+        // waited for here and so always before this tile's PV is issued (no
+        // waiter falls two phases behind on bar_o)
+        if (gj >= 2) {
+          if (!pf_wait_outlined(&bar_o[buf], (uint32_t)(((gj - 2) >> 1) & 1), &abort_flag, 12)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        const uint32_t pcol = lane_addr + C::P_COL + static_cast<uint32_t>(buf * 64);
+        const float neg_m = m_run == -CUDART_INF_F ? 0.f : -m_run;
+        const uint64_t c2 = f2_make(c, c), nm2 = f2_make(neg_m, neg_m);
+        uint64_t sum2 = f2_make(0.f, 0.f);
+        float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // rounded weights, 8 chains
+        uint32_t pk[16];
+        auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 e = f2_split(f2_fma(f2_make_u(r[2 * k], r[2 * k + 1]), c2, nm2));
+            const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+            pk[k] = pack_half2<kBf16>(p0, p1);
+            sum2 = f2_add(sum2, f2_make(p0, p1));
+            // O is normalised by the sum of the rounded weights it was built
+            // from, so O / l is a weighted mean with consistent weights
+            add_half2_to_f32<kBf16>(sr[2 * (k & 3)], sr[2 * (k & 3) + 1], pk[k]);
+          }
+          tmem_st16(pcol + col, pk);
+        };
+        // P(j) for keys [64 half, 64 half + 64) goes to its columns [32 half, 32 half + 32)
+        pack_chunk(r0, half * 32);
+        pack_chunk(r1, half * 32 + 16);
+        const float2 sv = f2_split(sum2);
+        l_run += sv.x + sv.y;
+        lr_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
+
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // the previous PV must be complete before O is rescaled.  The PV before
+          // it, on the same barrier, was waited for above one tile ago, so this
+          // wait is never more than one phase behind, and tiles that need no
+          // rescale need not wait.
+          if (!pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 7)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
+            tmem_ld32(oa, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(oa, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) signal(&bar_p[buf], p_remote[buf]);
+      }
+      if (ok && n > 0) {
+        // the item's last P.V (the earlier ones are done or finish before it)
+        ok = pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8);
+        tc_fence_after_sync();
+      }
+      // the row's sums are split over the two halves (one exchange buffer per
+      // item parity: a half cannot get two epilogues ahead of its partner)
+      const int ep = n_ep & 1;
+      xch_l[ep][half][row] = l_run;
+      xch_lr[ep][half][row] = lr_run;
+      mbar_arrive(&bar_xe[wq]);
+      if (ok) ok = pf_wait_outlined(&bar_xe[wq], (uint32_t)ep, &abort_flag, 10);
+      ++n_ep;
+      l_run += xch_l[ep][half ^ 1][row];
+      lr_run += xch_lr[ep][half ^ 1][row];
+      if (ok) {
+        const bool row_valid = q_row < q_hi;
+        const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
+        const size_t lse_idx = ((size_t)b * p.h_q + h) * p.S_q + q_row;
+        constexpr float kLn2 = 0.693147180559945309f;
+        if constexpr (kMode != kModePartial) {
+          const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + half * HD;
+          const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            if (n > 0) {
+              tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
+              tmem_ld_wait(o);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = 0u;
+            }
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              w[k] = pack_half2<kBf16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+            if (row_valid) {
+              // a warp's store touches 32 rows: 32-byte pieces halve the requests
+              // of 16-byte ones (the output's base decides)
+              if (o_v8) {
+                st_global_v8(orow + cc * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                st_global_v8(orow + cc * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                  dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+              }
+            }
+          }
+          if (p.lse != nullptr && row_valid && half == 0)
+            p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
+        } else {
+          const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
+          const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
+          // O re-weighted so that O / l equals the consistently normalised O_acc / lr
+          const float fo = any ? f * (l_run / lr_run) : 0.f;
+          float* orow = p.o_part + row_idx * D + half * HD;
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            if (n > 0) {
+              tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
+              tmem_ld_wait(o);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = 0u;
+            }
+            if (row_valid) {
+              float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
+                                      __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
+            }
+          }
+          if (row_valid && half == 0) {
+            p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
+            p.l_out[lse_idx] = any ? l_run * f : 0.f;
+          }
+        }
+      }
+    }  // items
+  }
+
+  // ------------------------------------------------------------ teardown
+  // Every thread of this CTA is done with TMEM and with signalling the other
+  // CTA.  The two CTAs then meet (bounded): neither exits, nor frees the
+  // pair's TMEM, while the other may still signal its barriers.
+  tc_fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive_remote(mapa_shared(&bar_exit, rank ^ 1u));
+    pf_drain(&bar_exit, 0);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_cta2(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool kBf16, int kMode, bool kOneChunk>
+attn_status_t launch_cta2_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
+  using C = Cta2Cfg;
+  auto kern = prefill_cta2_kernel<kBf16, kMode, kOneChunk>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (grid.x == 0 || grid.x % 2 != 0) return ATTN_ERR_INVALID_ARG;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Dense and window launches with one chunk, and every partial and jagged
+// launch (always one KV range), take the single-chunk instantiations.
+template <bool kBf16>
+attn_status_t launch_cta2_typed(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                const CUtensorMap& mv, int mode, dim3 grid, cudaStream_t s) {
+  const bool one = p.num_chunks == 1;
+  switch (mode) {
+    case kModeDense:
+      return one ? launch_cta2_variant<kBf16, kModeDense, true>(p, mq, mk, mv, grid, s)
+                 : launch_cta2_variant<kBf16, kModeDense, false>(p, mq, mk, mv, grid, s);
+    case kModeWindow:
+      return one ? launch_cta2_variant<kBf16, kModeWindow, true>(p, mq, mk, mv, grid, s)
+                 : launch_cta2_variant<kBf16, kModeWindow, false>(p, mq, mk, mv, grid, s);
+    case kModePartial:
+      return one ? launch_cta2_variant<kBf16, kModePartial, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+    case kModeJagged:
+      return one ? launch_cta2_variant<kBf16, kModeJagged, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_ERR_INVALID_ARG;
+}
+
+inline attn_status_t launch_cta2_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                          const CUtensorMap& mv, int mode, bool bf16, dim3 grid, cudaStream_t s) {
+  return bf16 ? launch_cta2_typed<true>(p, mq, mk, mv, mode, grid, s)
+              : launch_cta2_typed<false>(p, mq, mk, mv, mode, grid, s);
+}
+
+}  // namespace attn

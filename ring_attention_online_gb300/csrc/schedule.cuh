@@ -175,4 +175,15 @@ struct LinearWalk {
   }
 };
 
+// Work units of a head-dim-256 dense / partial / window launch, which runs on
+// CTA pairs: a pair item is 256 query rows (two consecutive 128-row Q tiles of
+// one head, or with pair_heads one Q tile of two query heads), and a unit is
+// up to two items of one (batch, head or head pair).
+__host__ __device__ inline long long cta2_units(int B, int S_q, int h_q, int pair_heads) {
+  const int n_qt = (S_q + 127) / 128;
+  const int n_it = pair_heads ? n_qt : (n_qt + 1) / 2;
+  const int n_y = pair_heads ? h_q / 2 : h_q;
+  return (long long)((n_it + 1) / 2) * n_y * B;
+}
+
 }  // namespace attn

@@ -357,9 +357,10 @@ def test_jagged_parity_and_worklist(causal, D, dtype):
     O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), causal)
     close_o(o, O, f"attn_jagged D={D} causal={causal} {dtype}")
     close_lse(lse, L)
-    # worklist: the same items as the oracle's flattened worklist, bit for bit.  Head
-    # dims 64/128 run two 128-row sub-tiles per CTA, so their Q tiles are 256 rows.
-    block_m = 256 if D <= 128 else 128
+    # worklist: the same items as the oracle's flattened worklist, bit for bit.  Every
+    # head dim runs two 128-row sub-tiles per item (head dims 64/128 in one CTA, 256 on
+    # a CTA pair), so the Q tiles are 256 rows.
+    block_m = 256
     words = ws.view(torch.int32).cpu().numpy()
     count = int(words[0])
     items = words[4:4 + 4 * count].reshape(count, 4)
