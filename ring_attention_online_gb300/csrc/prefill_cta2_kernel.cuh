@@ -39,12 +39,11 @@
 // CTA layout (352 threads; both CTAs of the pair run the same roles except
 // where noted):
 //   warp 0      TMA producer: this CTA's Q tile, then its halves of the K and V
-//               slabs through a K ring and a V ring of shared-memory stages,
-//               each copy completing on this CTA's own barrier.
-//   warp 1      rank 0: TMEM owner and S issuer, S(j) = Q.K_j^T for the pair.
-//               rank 1: TMEM owner and relay: forwards each completed copy of
-//               its CTA (Q and every slab) to rank 0 by a remote mbarrier
-//               arrival, so the issuers know both halves have landed.
+//               tiles through a K ring and a V ring of shared-memory stages.
+//               The copies of both CTAs complete on rank 0's barriers
+//               (cta_group::2 form), which rank 0 arms for the bytes of both,
+//               so one wait tells an issuer that both halves have landed.
+//   warp 1      TMEM owner; rank 0: S issuer, S(j) = Q.K_j^T for the pair.
 //   warp 10     rank 0: P.V issuer.  rank 1: idle.
 //   warps 2..9  softmax + epilogue of this CTA's 128 rows, two warps per row (a
 //               half of the tile's keys and of O's columns each), exactly as in
@@ -52,9 +51,11 @@
 //               go to rank 0's barriers (one arrival per warp).
 // Every MMA commit is multicast to both CTAs' barriers.  Every wait is bounded:
 // a timeout sets the library's device status, the CTA skips its remaining
-// work, drains its own copies and (rank 0) its MMAs, and both CTAs meet at a
-// bounded exit handshake before freeing TMEM, so neither leaves while the
-// other may still signal it.
+// work, waits for its copies in flight (rank 0 on its barriers; rank 1, whose
+// copies complete on rank 0's barriers, for a fixed time far longer than a
+// copy takes) and (rank 0) for its MMAs, and both CTAs meet at a bounded exit
+// handshake before freeing TMEM, so neither leaves while the other may still
+// signal it.
 #pragma once
 
 #include <math_constants.h>
@@ -67,49 +68,63 @@ struct Cta2Cfg {
   static constexpr int D = 256;
   static constexpr int BM = 128;                // query rows per CTA (256 per pair)
   static constexpr int BN = 128;                // keys per KV tile
-  static constexpr int SC = 128;                // columns of D per K or V slab
-  static constexpr int NH = D / SC;             // slabs per K or V tile
-  static constexpr int KH = BN / 2;             // keys of a K slab each CTA holds
-  static constexpr int VH = SC / 2;             // columns of a V slab each CTA holds
+  static constexpr int SC = 128;                // columns of D per P.V MMA (a half of D)
+  static constexpr int NH = D / SC;             // halves of D
+  static constexpr int KH = BN / 2;             // keys of a K tile each CTA holds
+  static constexpr int VH = SC / 2;             // columns of each half of D of V each CTA holds
   static constexpr int Q_BLOCK = 128 * 128;     // Q: 128 rows x 64 columns (128 B, swizzled)
   static constexpr int K_BLOCK = KH * 128;      // K half: 64 keys x 64 columns
+  static constexpr int V_BLOCK = BN * 128;      // V: 128 keys x 64 columns
   static constexpr int Q_BYTES = BM * D * 2;    // 64 KB
-  static constexpr int STAGE_BYTES = 16384;     // K half slab 64 x 128, V half slab 128 x 64
-  static constexpr int RING = 4;                // stages per ring: two tiles of K, two of V
+  // one stage per K or V tile: this CTA's 64 keys x 256 columns of K, or the
+  // tile's 128 keys x this CTA's 2 x 64 columns of V (one 64-column block per
+  // 128-column half of D).  One barrier per tile: each wait of an MMA issuer
+  // costs the tensor pipe a bubble (the wait holds the issuing thread until its
+  // MMAs drain), and with one wait per slab (two per tile) the kernel ran
+  // 1428-1510 vs 1471-1558 TFLOP/s on dense causal B=8 H=32 S=4096.
+  static constexpr int STAGE_BYTES = 32768;
+  static constexpr int RING = 2;                // stages per ring: two tiles of K, two of V
   static constexpr int NST = 2 * RING;
-  // + 1 KB alignment slack, + one stage of slack after the last stage: an MMA
-  // operand span never reaches past the CTA's allocation
-  static constexpr int SMEM_BYTES = Q_BYTES + NST * STAGE_BYTES + 1024 + STAGE_BYTES;
+  static constexpr int SMEM_BYTES = Q_BYTES + NST * STAGE_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM (each CTA, its own 128 rows): S(j) in [0, 128); P(j) (16-bit) in
   // [P_COL + 64 (j % 2), +64); O in [O_COL, O_COL + 256)
   static constexpr uint32_t P_COL = 128;
   static constexpr uint32_t O_COL = 256;
-  static constexpr int THREADS = 352;
+  // softmax warps per query row: 2 (64 keys and 128 O columns each); 4 measured
+  // slower (1364 vs 1428 TFLOP/s on dense causal B=8 H=32 S=4096)
+  static constexpr int WPR = 2;
+  static constexpr int SM_WARPS = 4 * WPR;      // softmax warps: WPR per TMEM lane quarter
+  static constexpr int KW = BN / WPR;           // keys of a tile per softmax warp
+  static constexpr int OW = D / WPR;            // O columns per softmax warp
+  static constexpr int PV_WARP = 2 + SM_WARPS;  // the P.V issuer's warp (rank 0)
+  static constexpr int THREADS = 32 * (3 + SM_WARPS);
   static constexpr uint16_t kBoth = 3;          // multicast mask of a commit: both CTAs
-  static constexpr uint32_t kSignals = 16;      // arrivals per phase: the pair's 16 softmax warps
-  static_assert(KH * SC * 2 == STAGE_BYTES && BN * VH * 2 == STAGE_BYTES, "stage size");
+  static constexpr uint64_t kPeerCopyDrainNs = 200000;  // rank 1's wait for its copies after an abort
+  static constexpr uint32_t kSignals = 2 * SM_WARPS;  // arrivals per phase: every softmax warp of the pair
+  static_assert(WPR == 2 || WPR == 4, "softmax warps per row");
+  static_assert(KH * D * 2 == STAGE_BYTES && BN * VH * 2 * NH == STAGE_BYTES, "stage size");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
-  static_assert(SMEM_BYTES + 8 * 1024 <= 227 * 1024, "shared memory budget (static part ~7 KB)");
+  static_assert(SMEM_BYTES + 13 * 1024 <= 227 * 1024, "shared memory budget (static part < 13 KB)");
 };
 
 template <bool kBf16, int kMode, bool kOneChunk>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
     prefill_cta2_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
   using C = Cta2Cfg;
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_pq, bar_qe, bar_fin, bar_exit;
+  __shared__ uint64_t bar_q, bar_qe, bar_fin, bar_exit;
   __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2] (both CTAs)
-  __shared__ uint64_t bar_full[C::NST], bar_pfull[C::NST], bar_empty[C::NST];
+  __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
   __shared__ uint64_t bar_s[2], bar_p[2];
   __shared__ uint64_t bar_sfree[2];  // the pair's softmax warps have read S(j) out of TMEM (j % 2)
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
-  __shared__ float xch_max[2][2][128];                   // [tile parity][column half][row]
-  __shared__ float xch_l[2][2][128], xch_lr[2][2][128];  // [item parity][column half][row]
-  __shared__ uint64_t bar_x[2][4];                       // pair-of-warps exchange: [tile parity][lane quarter]
+  __shared__ float xch_max[2][C::WPR][128];                       // [tile parity][key part][row]
+  __shared__ float xch_l[2][C::WPR][128], xch_lr[2][C::WPR][128];  // [item parity][key part][row]
+  __shared__ uint64_t bar_x[2][4];  // exchange of a row's warps: [tile parity][lane quarter]
   __shared__ uint64_t bar_xe[4];                         // end-of-row exchange per lane quarter
 
   const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs of the pair
@@ -202,7 +217,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
-    mbar_init(&bar_pq, 1);
     mbar_init(&bar_qe, 1);
     mbar_init(&bar_o[0], 1);
     mbar_init(&bar_o[1], 1);
@@ -210,16 +224,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
     mbar_init(&bar_exit, 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_pfull[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
       mbar_init(&bar_sfree[i], C::kSignals);
       mbar_init(&bar_p[i], C::kSignals);
-      for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 64);
+      for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 32 * C::WPR);
     }
-    for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_xe[q4], 64);
+    for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_xe[q4], 32 * C::WPR);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -239,30 +252,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
-      int filled[2] = {0, 0};  // slabs issued into the K ring and the V ring
+      int filled[2] = {0, 0};  // tiles issued into the K ring and the V ring
       int q_loads = 0;
       bool ok = true;
       int hk = 0, bb = 0;
       // fill f of a ring goes to its stage f % RING, once the pair's MMAs have
-      // released fill f - RING of that stage (the commit reaches both CTAs)
+      // released fill f - RING of that stage (the commit reaches both CTAs).
+      // Both CTAs' copies of a fill complete on rank 0's barrier, which rank 0
+      // arms for the bytes of both.
       auto push_tile = [&](int ring, int kstart) -> bool {
         int& fills = filled[ring];
-        for (int hs = 0; hs < C::NH; ++hs, ++fills) {
-          const int stage = ring * C::RING + fills % C::RING;
-          const uint32_t phase = (uint32_t)((fills / C::RING) & 1);
-          if (!pf_wait_outlined(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
-          uint8_t* dst = sKV + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&bar_full[stage], C::STAGE_BYTES);
-          if (ring == 0) {
-            // K: this CTA's 64 keys of the tile, the slab's 128 columns
-            for (int blk = 0; blk < C::SC / 64; ++blk)
-              tma_load_4d(dst + blk * C::K_BLOCK, &mk, &bar_full[stage], hs * C::SC + blk * 64, hk,
-                          kstart + C::KH * (int)rank, bb);
-          } else {
-            // V: the tile's 128 keys, this CTA's 64 columns of the slab
-            tma_load_4d(dst, &mv, &bar_full[stage], hs * C::SC + C::VH * (int)rank, hk, kstart, bb);
-          }
+        const int stage = ring * C::RING + fills % C::RING;
+        const uint32_t phase = (uint32_t)((fills / C::RING) & 1);
+        if (!pf_wait_outlined(&bar_empty[stage], phase ^ 1u, &abort_flag, 1)) return false;
+        uint8_t* dst = sKV + stage * C::STAGE_BYTES;
+        if (rank == 0) mbar_arrive_expect_tx(&bar_full[stage], 2 * C::STAGE_BYTES);
+        const uint32_t full0 = mapa_shared(&bar_full[stage], 0);
+        if (ring == 0) {
+          // K: this CTA's 64 keys of the tile, all 256 columns
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_4d_pair(dst + blk * C::K_BLOCK, &mk, full0, blk * 64, hk, kstart + C::KH * (int)rank, bb);
+        } else {
+          // V: the tile's 128 keys, this CTA's 64 columns of each 128-column half
+          for (int hs = 0; hs < C::NH; ++hs)
+            tma_load_4d_pair(dst + hs * C::V_BLOCK, &mv, full0, hs * C::SC + C::VH * (int)rank, hk, kstart, bb);
         }
+        ++fills;
         return true;
       };
       for (int i = 0; ok && i < n_my; ++i) {
@@ -278,9 +293,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
+        if (rank == 0) mbar_arrive_expect_tx(&bar_q, 2 * C::Q_BYTES);
+        const uint32_t q0 = mapa_shared(&bar_q, 0);
         for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(sQ + blk * C::Q_BLOCK, &mq, &bar_q, blk * 64, it.h, it.q_lo, it.b);
+          tma_load_4d_pair(sQ + blk * C::Q_BLOCK, &mq, q0, blk * 64, it.h, it.q_lo, it.b);
         ++q_loads;
         TileWalk kw = walk, vw = walk;
         int ch, st, me;
@@ -297,81 +313,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
         }
       }
       if (abort_flag) {
-        // this CTA's copies may still be landing in its shared memory: wait for them
-        if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
-        for (int ring = 0; ring < 2; ++ring) {
-          const int outstanding = filled[ring] < C::RING ? filled[ring] : C::RING;
-          for (int i = 0; i < outstanding; ++i) {
-            const int pos = filled[ring] - 1 - i;
-            pf_drain(&bar_full[ring * C::RING + pos % C::RING], (uint32_t)((pos / C::RING) & 1));
+        // copies may still be landing in this CTA's shared memory: wait for them
+        if (rank == 0) {
+          // rank 0's barriers see the copies of both CTAs (a fill that rank 1
+          // never issued leaves its phase open: that wait gives up, bounded)
+          if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
+          for (int ring = 0; ring < 2; ++ring) {
+            const int outstanding = filled[ring] < C::RING ? filled[ring] : C::RING;
+            for (int i = 0; i < outstanding; ++i) {
+              const int pos = filled[ring] - 1 - i;
+              pf_drain(&bar_full[ring * C::RING + pos % C::RING], (uint32_t)((pos / C::RING) & 1));
+            }
+          }
+        } else {
+          // rank 1's copies complete on rank 0's barriers, which it cannot poll:
+          // it waits far longer than a copy takes (rank 0 waits for it at the
+          // exit handshake, so its barriers outlive the copies)
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < C::kPeerCopyDrainNs) {
           }
         }
       }
     }
   } else if (warp == 1 && rank != 0) {
-    // ========================================================== relay (rank 1)
-    // Forwards, in the producer's order, each completed copy of this CTA to the
-    // matching barrier of rank 0 (bar_pq for Q, bar_pfull for a slab).
-    if (lane == 0) {
-      const uint32_t pq_remote = mapa_shared(&bar_pq, 0);
-      int filled[2] = {0, 0};
-      int q_loads = 0;
-      bool ok = true;
-      auto relay_tile = [&](int ring) -> bool {
-        for (int hs = 0; hs < C::NH; ++hs) {
-          const int f = filled[ring]++;
-          const int stage = ring * C::RING + f % C::RING;
-          if (!pf_wait_outlined(&bar_full[stage], (uint32_t)((f / C::RING) & 1), &abort_flag, 14)) return false;
-          mbar_arrive_remote(mapa_shared(&bar_pfull[stage], 0));
-        }
-        return true;
-      };
-      for (int i = 0; ok && i < n_my; ++i) {
-        const Item it = get_item(i);
-        if (!it.valid) continue;
-        TileWalk walk;
-        const int n = item_walk(it, walk);
-        if (n == 0) continue;
-        ok = pf_wait_outlined(&bar_q, (uint32_t)(q_loads & 1), &abort_flag, 15);
-        if (!ok) break;
-        mbar_arrive_remote(pq_remote);
-        ++q_loads;
-        ok = relay_tile(0);
-        for (int j = 0; ok && j < n; ++j) {
-          if (j + 1 < n) {
-            ok = relay_tile(0);
-            if (!ok) break;
-          }
-          ok = relay_tile(1);
-        }
-      }
-      // rank 0's MMAs read this CTA's shared memory and write its TMEM: they
-      // finish before this CTA tears down (the final commits reach both CTAs)
-      pf_drain(&bar_fin, 0);
-    }
-  } else if (warp == 1 || warp == 10) {
+    // ========================================================== rank 1, warp 1
+    // rank 0's MMAs read this CTA's shared memory and write its TMEM: they
+    // finish before this CTA tears down (the final commits reach both CTAs)
+    if (lane == 0) pf_drain(&bar_fin, 0);
+  } else if (warp == 1 || warp == C::PV_WARP) {
     // ========================================================== MMA issuers (rank 0)
-    // Warp 1 issues S(j), warp 10 PV(j), for the whole pair.  Each only waits
-    // on work of other roles (a wait stalls until the thread's own issued
-    // tcgen05 work has drained): the S issuer on K slabs and on the softmax
-    // having read S(j-1); the PV issuer on P(j) and V slabs.  A slab is ready
-    // when both CTAs' halves have landed: this CTA's copy completes bar_full,
-    // rank 1's is relayed to bar_pfull.
+    // Warp 1 issues S(j), warp PV_WARP PV(j), for the whole pair.  Each only
+    // waits on work of other roles, twice per tile (a wait stalls until the
+    // thread's own issued tcgen05 work has drained, a bubble in the tensor
+    // pipe): the S issuer on the softmax having read S(j-1) and on K(j), the PV
+    // issuer on P(j) and on V(j).
     if (lane == 0 && rank == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(256, C::BN, kBf16, false);
       constexpr uint32_t kIdescPV = idesc_f16_f32acc(256, C::SC, kBf16, true);
       const uint32_t skv = smem_u32(sKV);
-      auto wait_slab = [&](int ring, int f, uint32_t site) -> bool {
+      auto wait_tile = [&](int ring, int f, uint32_t site) -> bool {
         const int stage = ring * C::RING + f % C::RING;
         const uint32_t ph = (uint32_t)((f / C::RING) & 1);
         if (!pf_wait_outlined(&bar_full[stage], ph, &abort_flag, site)) return false;
-        if (!pf_wait_outlined(&bar_pfull[stage], ph, &abort_flag, site)) return false;
         tc_fence_after_sync();
         return true;
       };
       bool ok = true;
       int g = 0;          // S (or PV) groups issued so far, all items: barrier phases
-      int slab_base = 0;  // slabs of this issuer's ring taken by the earlier items
+      int tile_base = 0;  // tiles of this issuer's ring taken by the earlier items
       int q_used = 0;     // Q tiles consumed (S issuer)
       for (int i = 0; ok && i < n_my; ++i) {
         const Item it = get_item(i);
@@ -381,8 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
         if (n == 0) continue;
         if (warp == 1) {
           const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-          ok = pf_wait_outlined(&bar_q, (uint32_t)(q_used & 1), &abort_flag, 5) &&
-               pf_wait_outlined(&bar_pq, (uint32_t)(q_used & 1), &abort_flag, 5);
+          ok = pf_wait_outlined(&bar_q, (uint32_t)(q_used & 1), &abort_flag, 5);
           tc_fence_after_sync();
           ++q_used;
           for (int j = 0; ok && j < n; ++j, ++g) {
@@ -392,20 +380,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
               if (!ok) break;
               tc_fence_after_sync();
             }
-            for (int hs = 0; hs < C::NH; ++hs) {
-              const int sl = slab_base + j * C::NH + hs;
-              ok = wait_slab(0, sl, 2);
+            {
+              const int tl = tile_base + j;
+              ok = wait_tile(0, tl, 2);
               if (!ok) break;
-              const uint64_t kdesc = smem_desc_sw128(skv + (sl % C::RING) * C::STAGE_BYTES, 16, 1024);
+              const uint64_t kdesc = smem_desc_sw128(skv + (tl % C::RING) * C::STAGE_BYTES, 16, 1024);
 #pragma unroll
-              for (int ks = 0; ks < C::SC / 16; ++ks) {
+              for (int ks = 0; ks < D / 16; ++ks) {
                 // 16 columns of D per MMA: 32 bytes inside a 128-byte swizzle row,
                 // the next 64-column block every four steps
-                const uint32_t qoff = (hs * (C::SC / 64) + ks / 4) * C::Q_BLOCK + (ks % 4) * 32;
+                const uint32_t qoff = (ks / 4) * C::Q_BLOCK + (ks % 4) * 32;
                 const uint32_t koff = (ks / 4) * C::K_BLOCK + (ks % 4) * 32;
-                mma_ss_cta2(tmem, desc_advance(qdesc, qoff), desc_advance(kdesc, koff), kIdescS, (hs | ks) != 0);
+                mma_ss_cta2(tmem, desc_advance(qdesc, qoff), desc_advance(kdesc, koff), kIdescS, ks != 0);
               }
-              mma_commit_cta2(&bar_empty[sl % C::RING], C::kBoth);
+              mma_commit_cta2(&bar_empty[tl % C::RING], C::kBoth);
             }
             if (!ok) break;
             mma_commit_cta2(&bar_s[g & 1], C::kBoth);
@@ -419,41 +407,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
             tc_fence_after_sync();  // P of both CTAs in TMEM
             const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((g & 1) * 64);
             const uint32_t acc0 = j > 0 ? 1u : 0u;  // the item's first PV starts O afresh
-            for (int hs = 0; hs < C::NH; ++hs) {
-              const int sl = slab_base + j * C::NH + hs;
-              ok = wait_slab(1, sl, 4);
+            {
+              const int tl = tile_base + j;
+              ok = wait_tile(1, tl, 4);
               if (!ok) break;
-              const int stage = C::RING + sl % C::RING;
-              const uint64_t vdesc = smem_desc_sw128(skv + stage * C::STAGE_BYTES, 16384, 1024);
-              // 16 keys of V per MMA (16 rows of 128 bytes)
+              const int stage = C::RING + tl % C::RING;
+              for (int hs = 0; hs < C::NH; ++hs) {
+                const uint64_t vdesc = smem_desc_sw128(skv + stage * C::STAGE_BYTES + hs * C::V_BLOCK, 16384, 1024);
+                // 16 keys of V per MMA (16 rows of 128 bytes)
 #pragma unroll
-              for (int ks = 0; ks < C::BN / 16; ++ks)
-                mma_ts_cta2(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
-                            ks > 0 ? 1u : acc0);
+                for (int ks = 0; ks < C::BN / 16; ++ks)
+                  mma_ts_cta2(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                              ks > 0 ? 1u : acc0);
+              }
               mma_commit_cta2(&bar_empty[stage], C::kBoth);
             }
             if (!ok) break;
             mma_commit_cta2(&bar_o[g & 1], C::kBoth);
           }
         }
-        slab_base += n * C::NH;
+        tile_base += n;
       }
       // every MMA either issuer issued must finish before TMEM is released (both CTAs)
       mma_commit_cta2(&bar_fin, C::kBoth);
       pf_drain(&bar_fin, 0);
     }
-  } else if (warp >= 2 && warp <= 9) {
+  } else if (warp >= 2 && warp < 2 + C::SM_WARPS) {
     // ========================================================== softmax + epilogue (both CTAs)
-    // Two warps share each TMEM lane quarter: warp (2 + wq) and (6 + wq) take the
-    // two column halves of every row (keys [64 half, 64 half + 64) of a tile, O
-    // columns [half D/2, half D/2 + D/2)).  The two exchange row maxima once per
-    // tile through shared memory, so both halves take identical decisions.
-    const int sw = warp - 2;  // 0..7
-    const int wq = warp & 3;  // TMEM lane quarter this warp may access
-    const int half = sw >> 2;
+    // WPR warps share each TMEM lane quarter: warp 2 + 4 kq + (wq - 2) mod 4 ...
+    // takes key part kq of every row of lane quarter wq (keys [KW kq, KW kq + KW)
+    // of a tile, O columns [OW kq, OW kq + OW)).  The row's warps exchange their
+    // maxima once per tile through shared memory, so all take identical
+    // decisions.
+    constexpr int KW = C::KW, OW = C::OW, NKC = KW / 32;
+    const int sw = warp - 2;        // 0 .. SM_WARPS - 1
+    const int wq = warp & 3;        // TMEM lane quarter this warp may access
+    const int kq = sw >> 2;         // key part of this warp
     const int row = wq * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    constexpr int HD = D / 2;  // O columns per half
     const float c = p.scale_log2;  // > 0
     const uint32_t sfree_remote[2] = {mapa_shared(&bar_sfree[0], 0), mapa_shared(&bar_sfree[1], 0)};
     const uint32_t p_remote[2] = {mapa_shared(&bar_p[0], 0), mapa_shared(&bar_p[1], 0)};
@@ -475,8 +466,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
       const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
       const int q_row = q_lo + row;
       float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
-      float l_run = 0.f;             // this half's sum of exp2(x - m_run) in fp32: l and LSE
-      float lr_run = 0.f;            // this half's sum of the rounded P the MMA multiplies V by
+      float l_run = 0.f;             // this part's sum of exp2(x - m_run) in fp32: l and LSE
+      float lr_run = 0.f;            // this part's sum of the rounded P the MMA multiplies V by
       float m_max = -CUDART_INF_F;   // true running max (partial mode)
       for (int j = 0; j < n; ++j, ++gj) {
         int ch, kstart, mend;
@@ -487,11 +478,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
           break;
         }
         tc_fence_after_sync();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(lane_addr + half * 64, r0);
-        tmem_ld32(lane_addr + half * 64 + 32, r1);
-        tmem_ld_wait(r0);
-        tmem_ld_wait(r1);
+        uint32_t r[NKC][32];
+#pragma unroll
+        for (int cc = 0; cc < NKC; ++cc) tmem_ld32(lane_addr + kq * KW + cc * 32, r[cc]);
+#pragma unroll
+        for (int cc = 0; cc < NKC; ++cc) tmem_ld_wait(r[cc]);
         // S(j) is in registers: the S issuer may overwrite the buffer with S(j+1)
         tc_fence_before_sync();
         __syncwarp();
@@ -513,31 +504,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
             lim = lc < lim ? lc : lim;
             if (win) flo = lc - 1 - p.window;
           }
-          const long long lh = lim - half * 64, fh = flo - half * 64;  // limits within this half
+          const long long lh = lim - kq * KW, fh = flo - kq * KW;  // limits within this part
           const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (k >= lh || k < fh) r0[k] = ninf;
-            if (k + 32 >= lh || k + 32 < fh) r1[k] = ninf;
-          }
+          for (int cc = 0; cc < NKC; ++cc)
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (cc * 32 + k >= lh || cc * 32 + k < fh) r[cc][k] = ninf;
         }
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          mx8[k] = fmax3(__uint_as_float(r0[k]), __uint_as_float(r0[k + 8]), __uint_as_float(r0[k + 16]));
-          mx8[k] = fmax3(mx8[k], __uint_as_float(r0[k + 24]), __uint_as_float(r1[k]));
-          mx8[k] = fmax3(mx8[k], __uint_as_float(r1[k + 8]), __uint_as_float(r1[k + 16]));
-          mx8[k] = fmaxf(mx8[k], __uint_as_float(r1[k + 24]));
+          mx8[k] = fmax3(__uint_as_float(r[0][k]), __uint_as_float(r[0][k + 8]), __uint_as_float(r[0][k + 16]));
+          mx8[k] = fmaxf(mx8[k], __uint_as_float(r[0][k + 24]));
+#pragma unroll
+          for (int cc = 1; cc < NKC; ++cc) {
+            mx8[k] = fmax3(mx8[k], __uint_as_float(r[cc][k]), __uint_as_float(r[cc][k + 8]));
+            mx8[k] = fmax3(mx8[k], __uint_as_float(r[cc][k + 16]), __uint_as_float(r[cc][k + 24]));
+          }
         }
         float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-        // both halves of the row see each other's max
-        xch_max[buf][half][row] = mx;
+        // the row's parts see each other's max
+        xch_max[buf][kq][row] = mx;
         mbar_arrive(&bar_x[buf][wq]);
         if (!pf_wait_outlined(&bar_x[buf][wq], (uint32_t)((gj >> 1) & 1), &abort_flag, 9)) {
           ok = false;
           break;
         }
-        mx = fmaxf(mx, xch_max[buf][half ^ 1][row]);
+#pragma unroll
+        for (int o = 1; o < C::WPR; ++o) mx = fmaxf(mx, xch_max[buf][(kq + o) % C::WPR][row]);
         const float m_tile = mx * c;  // -inf when the whole row is masked
         if constexpr (kMode == kModePartial) m_max = fmaxf(m_max, m_tile);
         const float m_new = fmaxf(m_run, m_tile);
@@ -565,10 +560,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
         uint64_t sum2 = f2_make(0.f, 0.f);
         float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // rounded weights, 8 chains
         uint32_t pk[16];
-        auto pack_chunk = [&](uint32_t (&r)[32], uint32_t col) {
+        // P(j) for keys [KW kq, KW kq + KW) goes to its columns [KW / 2 kq, +KW / 2)
+#pragma unroll
+        for (int cc = 0; cc < NKC; ++cc) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float2 e = f2_split(f2_fma(f2_make_u(r[2 * k], r[2 * k + 1]), c2, nm2));
+            const float2 e = f2_split(f2_fma(f2_make_u(r[cc][2 * k], r[cc][2 * k + 1]), c2, nm2));
             const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
             pk[k] = pack_half2<kBf16>(p0, p1);
             sum2 = f2_add(sum2, f2_make(p0, p1));
@@ -576,11 +573,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
             // from, so O / l is a weighted mean with consistent weights
             add_half2_to_f32<kBf16>(sr[2 * (k & 3)], sr[2 * (k & 3) + 1], pk[k]);
           }
-          tmem_st16(pcol + col, pk);
-        };
-        // P(j) for keys [64 half, 64 half + 64) goes to its columns [32 half, 32 half + 32)
-        pack_chunk(r0, half * 32);
-        pack_chunk(r1, half * 32 + 16);
+          tmem_st16(pcol + kq * (KW / 2) + cc * 16, pk);
+        }
         const float2 sv = f2_split(sum2);
         l_run += sv.x + sv.y;
         lr_run += ((sr[0] + sr[1]) + (sr[2] + sr[3])) + ((sr[4] + sr[5]) + (sr[6] + sr[7]));
@@ -596,9 +590,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
           }
           tc_fence_after_sync();
 #pragma unroll 1
-          for (int cc = 0; cc < HD / 32; ++cc) {
+          for (int cc = 0; cc < OW / 32; ++cc) {
             uint32_t o[32];
-            const uint32_t oa = lane_addr + C::O_COL + half * HD + cc * 32;
+            const uint32_t oa = lane_addr + C::O_COL + kq * OW + cc * 32;
             tmem_ld32(oa, o);
             tmem_ld_wait(o);
 #pragma unroll
@@ -616,16 +610,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
         ok = pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8);
         tc_fence_after_sync();
       }
-      // the row's sums are split over the two halves (one exchange buffer per
-      // item parity: a half cannot get two epilogues ahead of its partner)
+      // the row's sums are split over its parts (one exchange buffer per item
+      // parity: a part cannot get two epilogues ahead of the others)
       const int ep = n_ep & 1;
-      xch_l[ep][half][row] = l_run;
-      xch_lr[ep][half][row] = lr_run;
+      xch_l[ep][kq][row] = l_run;
+      xch_lr[ep][kq][row] = lr_run;
       mbar_arrive(&bar_xe[wq]);
       if (ok) ok = pf_wait_outlined(&bar_xe[wq], (uint32_t)ep, &abort_flag, 10);
       ++n_ep;
-      l_run += xch_l[ep][half ^ 1][row];
-      lr_run += xch_lr[ep][half ^ 1][row];
+#pragma unroll
+      for (int o = 1; o < C::WPR; ++o) {
+        l_run += xch_l[ep][(kq + o) % C::WPR][row];
+        lr_run += xch_lr[ep][(kq + o) % C::WPR][row];
+      }
       if (ok) {
         const bool row_valid = q_row < q_hi;
         const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
@@ -633,13 +630,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
         constexpr float kLn2 = 0.693147180559945309f;
         if constexpr (kMode != kModePartial) {
           const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
-          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + half * HD;
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + kq * OW;
           const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll 1
-          for (int cc = 0; cc < HD / 32; ++cc) {
+          for (int cc = 0; cc < OW / 32; ++cc) {
             uint32_t o[32];
             if (n > 0) {
-              tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
+              tmem_ld32(lane_addr + C::O_COL + kq * OW + cc * 32, o);
               tmem_ld_wait(o);
             } else {
 #pragma unroll
@@ -663,19 +660,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
               }
             }
           }
-          if (p.lse != nullptr && row_valid && half == 0)
+          if (p.lse != nullptr && row_valid && kq == 0)
             p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
         } else {
           const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
           const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
           // O re-weighted so that O / l equals the consistently normalised O_acc / lr
           const float fo = any ? f * (l_run / lr_run) : 0.f;
-          float* orow = p.o_part + row_idx * D + half * HD;
+          float* orow = p.o_part + row_idx * D + kq * OW;
 #pragma unroll 1
-          for (int cc = 0; cc < HD / 32; ++cc) {
+          for (int cc = 0; cc < OW / 32; ++cc) {
             uint32_t o[32];
             if (n > 0) {
-              tmem_ld32(lane_addr + C::O_COL + half * HD + cc * 32, o);
+              tmem_ld32(lane_addr + C::O_COL + kq * OW + cc * 32, o);
               tmem_ld_wait(o);
             } else {
 #pragma unroll
@@ -689,7 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(352, 1)
                                       __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
             }
           }
-          if (row_valid && half == 0) {
+          if (row_valid && kq == 0) {
             p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
             p.l_out[lse_idx] = any ? l_run * f : 0.f;
           }
