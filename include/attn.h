@@ -60,7 +60,8 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement (e.g. D) */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, tensor map) */
   ATTN_ERR_TIMEOUT = 4,     /* a device-side wait gave up (reported by attn_last_device_status) */
-  ATTN_ERR_DEVICE_INPUT = 5 /* device-side input check failed, e.g. non-monotone seq_offsets */
+  ATTN_ERR_DEVICE_INPUT = 5, /* device-side input check failed, e.g. non-monotone seq_offsets */
+  ATTN_ERR_BOUNDS = 6        /* checked build: a kernel's index or tile coordinate left its extent */
 } attn_status_t;
 
 typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
@@ -215,10 +216,33 @@ attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const vo
 
 /*
  * attn_last_device_status - synchronise `stream`, then return and clear the
- * device-side status (ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_INPUT) raised by any
- * kernel of the library since the previous call; ATTN_OK if none.
+ * device-side status (ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_INPUT, ATTN_ERR_BOUNDS,
+ * in that order of precedence) raised by any kernel of the library since the
+ * previous call; ATTN_OK if none.
  */
 attn_status_t attn_last_device_status(attn_stream_t stream);
+
+/*
+ * Checked builds.  The same sources compiled with ATTN_CHECKED=1 give
+ * libattn_checked.so, a debug variant of this library: before every global
+ * store, every TMA tile load and every read of a worklist entry its kernels
+ * test the index or coordinate against the extent of its buffer (a tile's row
+ * start may lie up to two tiles past the last row: such boxes read zeros, which
+ * is how tail and empty tiles load).  A failed test records ATTN_ERR_BOUNDS in
+ * the device status and the access is skipped (a tile load takes tile 0
+ * instead), so the context stays usable.  No counterpart on the pages: it guards
+ * the library's own indexing (the failure class of DMA copies started out of
+ * step with their waits, which the ring-attention review thread warns about).
+ *
+ * attn_build_checked - 1 in the checked variant, 0 otherwise.
+ * attn_selftest_bounds - checked variant only (else ATTN_ERR_UNSUPPORTED, no
+ *   launch): one thread stores to index 1 of the one-element int buffer `buf`
+ *   (device memory, 4-byte aligned, owned by the caller) through the store
+ *   check, which records ATTN_ERR_BOUNDS and skips the store (buf is unchanged).
+ *   Read the result with attn_last_device_status().
+ */
+int attn_build_checked(void);
+attn_status_t attn_selftest_bounds(int* buf, attn_stream_t stream);
 
 /*
  * attn_selftest_wait_timeout - failure-detection self-test.  Launches one thread

@@ -23,14 +23,14 @@ __all__ = [
     "attn_prefill", "attn_prefill_window", "attn_partial", "attn_merge", "attn_jagged", "attn_decode_splitkv",
     "attn_jagged_workspace_bytes", "attn_decode_workspace_bytes", "attn_decode_splitkv_noalloc",
     "attn_last_device_status", "attn_status_string", "attn_tile_walk", "attn_selftest_wait_timeout",
-    "attn_probe_mma_cycles",
+    "attn_probe_mma_cycles", "attn_build_checked", "attn_selftest_bounds",
     "BLOCK_M", "BLOCK_N", "STATUS",
 ]
 
 BLOCK_M = 128
 BLOCK_N = 128
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
-          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_DEVICE_INPUT"}
+          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_DEVICE_INPUT", 6: "ATTN_ERR_BOUNDS"}
 _FP16, _BF16 = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +38,12 @@ _LIB = None
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, "libattn.so")
+    """libattn.so, or its checked debug variant libattn_checked.so when the
+    environment variable ATTN_LIBRARY is "checked" (see attn.h, "Checked builds")."""
+    variant = os.environ.get("ATTN_LIBRARY", "")
+    if variant not in ("", "default", "checked"):
+        raise ValueError(f"ATTN_LIBRARY={variant!r}: expected 'checked' or unset")
+    return os.path.join(_HERE, "libattn_checked.so" if variant == "checked" else "libattn.so")
 
 
 class AttnError(RuntimeError):
@@ -63,6 +68,8 @@ _SIGNATURES = {
     "attn_tile_walk": [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P],
     "attn_selftest_wait_timeout": [ctypes.c_uint64, _P],
     "attn_probe_mma_cycles": [_P, _I, _P],
+    "attn_build_checked": [],
+    "attn_selftest_bounds": [_P, _P],
 }
 
 
@@ -243,6 +250,21 @@ def attn_probe_mma_cycles(groups: int = 4096, stream=None) -> float:
     if gave_up:
         raise AttnError(4, "attn_probe_mma_cycles")
     return cycles / (8.0 * int(groups))
+
+
+def attn_build_checked() -> bool:
+    """True when the loaded library is the checked debug variant."""
+    return bool(load_library().attn_build_checked())
+
+
+def attn_selftest_bounds(buf, stream=None):
+    """Checked variant only: a store to index 1 of the one-element int32 CUDA tensor
+    `buf` through the store check (see attn.h); read the result with
+    attn_last_device_status()."""
+    import torch
+    _need(buf.is_cuda and buf.dtype == torch.int32 and buf.numel() == 1, "buf: one int32 CUDA element")
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(load_library().attn_selftest_bounds(_ptr(buf), ctypes.c_void_p(s.cuda_stream)), "attn_selftest_bounds")
 
 
 def attn_status_string(status: int) -> str:

@@ -4,6 +4,7 @@
 #include <math.h>
 #include <mutex>
 
+#include "checked.cuh"
 #include "common.cuh"
 #include "schedule.cuh"
 
@@ -334,15 +335,24 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, v
 attn_status_t attn_last_device_status(attn_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const unsigned int v = prefill_d64_take_status(s) | prefill_d128_take_status(s) | prefill_d256_take_status(s) |
-                         worklist_take_status(s) | decode_take_status(s);
+                         worklist_take_status(s) | decode_take_status(s) | merge_take_status(s);
   if (v & kStatusTimeout) return ATTN_ERR_TIMEOUT;
   if (v & kStatusDeviceInput) return ATTN_ERR_DEVICE_INPUT;
+  if (v & kStatusBounds) return ATTN_ERR_BOUNDS;
   return ATTN_OK;
 }
 
 attn_status_t attn_probe_mma_cycles(unsigned long long* cycles, int groups, attn_stream_t stream) {
   if (!cycles || !aligned(cycles, 8) || groups < 1 || groups > (1 << 20)) return ATTN_ERR_INVALID_ARG;
   return launch_probe_mma(cycles, groups, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_build_checked(void) { return ATTN_CHECKED ? 1 : 0; }
+
+attn_status_t attn_selftest_bounds(int* buf, attn_stream_t stream) {
+  if (!buf || !aligned(buf, 4)) return ATTN_ERR_INVALID_ARG;
+  if (!ATTN_CHECKED) return ATTN_ERR_UNSUPPORTED;
+  return launch_selftest_bounds(buf, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_selftest_wait_timeout(uint64_t timeout_ns, attn_stream_t stream) {
@@ -358,6 +368,7 @@ const char* attn_status_string(attn_status_t status) {
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
     case ATTN_ERR_DEVICE_INPUT: return "device-side input check failed";
+    case ATTN_ERR_BOUNDS: return "device-side bounds check failed (checked build)";
   }
   return "unknown status";
 }

@@ -14,6 +14,7 @@ namespace attn {
 enum : unsigned int {
   kStatusTimeout = 1u,       // some bounded wait gave up
   kStatusDeviceInput = 2u,   // malformed device-side input (seq_offsets)
+  kStatusBounds = 4u,        // checked builds: an index or tile coordinate out of its extent (access skipped)
   kStatusSiteShift = 8u,     // bits 8..23: which wait gave up (diagnostics)
 };
 
@@ -71,6 +72,7 @@ attn_status_t launch_worklist(const int32_t* seq_offsets, int num_seqs, int tota
                               int block_m, int* count_and_items, int max_items, cudaStream_t s);
 unsigned int worklist_take_status(cudaStream_t s);
 attn_status_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t s);
+attn_status_t launch_selftest_bounds(int* buf, cudaStream_t s);
 attn_status_t launch_probe_mma(unsigned long long* out, int groups, cudaStream_t s);
 
 // Split-KV decode partials; with `counters` (B * h_kv zeroed ints) the last
@@ -79,5 +81,6 @@ attn_status_t launch_decode_partial(const void* q, const CUtensorMap& mk, const 
                                     float* o, int B, int S_kv, int h_q, int h_kv, int D, bool bf16, float scale_log2,
                                     int num_splits, int* counters, void* out, float* lse, cudaStream_t s);
 unsigned int decode_take_status(cudaStream_t s);
+unsigned int merge_take_status(cudaStream_t s);
 
 }  // namespace attn

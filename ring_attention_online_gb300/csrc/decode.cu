@@ -23,6 +23,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "checked.cuh"
 #include "merge.cuh"
 #include "ptx.cuh"
 
@@ -160,8 +161,11 @@ __global__ void __launch_bounds__(160) decode_partial_kernel(const __grid_consta
         mbar_arrive_expect_tx(&bar_full[stage], C::STAGE_BYTES);
         const int key0 = k_lo + t * C::KEYS;
         for (int blk = 0; blk < D / 64; ++blk) {
-          tma_load_4d(dst + blk * C::BLOCK_BYTES, &mk, &bar_full[stage], blk * 64, g, key0, b);
-          tma_load_4d(dst + C::TILE_BYTES + blk * C::BLOCK_BYTES, &mv, &bar_full[stage], blk * 64, g, key0, b);
+          // a load whose coordinates fail the checked build's test loads tile 0
+          const bool c_ok = check_tile(blk * 64, g, key0, b, D, h_kv, S_kv, B, C::KEYS, &g_decode_status);
+          const int c0 = c_ok ? blk * 64 : 0, c1 = c_ok ? g : 0, c2 = c_ok ? key0 : 0, c3 = c_ok ? b : 0;
+          tma_load_4d(dst + blk * C::BLOCK_BYTES, &mk, &bar_full[stage], c0, c1, c2, c3);
+          tma_load_4d(dst + C::TILE_BYTES + blk * C::BLOCK_BYTES, &mv, &bar_full[stage], c0, c1, c2, c3);
         }
         ++issued;
         if (++stage == C::NST) {
@@ -333,6 +337,7 @@ __global__ void __launch_bounds__(160) decode_partial_kernel(const __grid_consta
       }
     }
     const size_t row = ((size_t)split * B + b) * h_q + (size_t)g * G + r;  // [C, B, h_q]
+    if (!check_index((long long)row, (long long)num_splits * B * h_q, &g_decode_status)) continue;
     o_out[row * D + d] = o;
     if (d == 0) {
       m_out[row] = M == -CUDART_INF_F ? -CUDART_INF_F : M * kLn2;
@@ -345,6 +350,7 @@ __global__ void __launch_bounds__(160) decode_partial_kernel(const __grid_consta
   // ============================================================ fused merge
   __threadfence();  // this CTA's partials are visible device-wide before it is counted
   __syncthreads();
+  if (!check_index((long long)b * h_kv + g, (long long)B * h_kv, &g_decode_status)) return;
   int* counter = counters + (size_t)b * h_kv + g;
   if (threadIdx.x == 0) last_of_group = atomicAdd(counter, 1) == num_splits - 1;
   __syncthreads();
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(160) decode_partial_kernel(const __grid_consta
   for (int r = warp; r < G; r += C::CONSUMERS + 1) {
     const size_t hrow = (size_t)b * h_q + (size_t)g * G + r;  // [B, h_q]: O is [B, h_q, D]
     merge_row<D, kBf16>(m_out, l_out, o_out, num_splits, ml_stride, hrow, ml_stride * D, hrow * D, out, lse, hrow,
-                        lane);
+                        lane, (long long)B * h_q, &g_decode_status);
   }
   if (threadIdx.x == 0) *counter = 0;  // ready for the next call on this workspace
 }

@@ -6,6 +6,8 @@
 
 namespace attn {
 
+static __device__ unsigned int g_merge_status;  // checked builds: store bounds
+
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ m, const float* __restrict__ l,
                                                     const float* __restrict__ o, int C, int B, int S_q, int H,
@@ -22,7 +24,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ m,
   const long long b = bs / S_q;
   const size_t ml_idx = ((size_t)b * H + h) * S_q + s;
   merge_row<D, kBf16>(m, l, o, C, (size_t)B * H * S_q, ml_idx, (size_t)rows * D, (size_t)row * D, out, lse, ml_idx,
-                      lane);
+                      lane, rows, &g_merge_status);
 }
 
 template <int D, bool kBf16>
@@ -47,6 +49,17 @@ attn_status_t launch_merge(const float* m, const float* l, const float* o, int C
                               : launch_merge_t<256, false>(m, l, o, C, B, S_q, H, out, lse, s);
   }
   return ATTN_ERR_UNSUPPORTED;
+}
+
+unsigned int merge_take_status(cudaStream_t s) {
+  if (cudaStreamSynchronize(s) != cudaSuccess) return kStatusTimeout;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_merge_status, sizeof(v)) != cudaSuccess) return kStatusTimeout;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_merge_status, &zero, sizeof(zero));
+  }
+  return v;
 }
 
 }  // namespace attn

@@ -12,6 +12,7 @@
 
 #include <math_constants.h>
 
+#include "checked.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -22,11 +23,14 @@ namespace attn {
 // D/32 contiguous columns, so every partial row is read once with coalesced
 // loads; the loads bypass L1 because the partials may have been written by
 // other CTAs of the same kernel.
+// out_rows: rows of `out` (and of `lse`); status: the calling kernel's status
+// word, for the checked build's store checks.
 template <int D, bool kBf16>
 __device__ __forceinline__ void merge_row(const float* __restrict__ m, const float* __restrict__ l,
                                           const float* __restrict__ o, int C, size_t ml_stride, size_t ml_idx,
                                           size_t o_stride, size_t o_idx, void* __restrict__ out,
-                                          float* __restrict__ lse, size_t lse_idx, int lane) {
+                                          float* __restrict__ lse, size_t lse_idx, int lane, long long out_rows,
+                                          unsigned int* status) {
   constexpr int PER = D / 32;
   const size_t col = o_idx + (size_t)lane * PER;
   float M = -CUDART_INF_F;
@@ -88,6 +92,8 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ m, const flo
 #pragma unroll
   for (int i = 0; i < PER / 2; ++i) packed[i] = pack_half2<kBf16>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
   uint16_t* dst = reinterpret_cast<uint16_t*>(out) + col;
+  if (!check_index((long long)(col / D), out_rows, status) || !check_index((long long)lse_idx, out_rows, status))
+    return;
   if constexpr (PER == 2) {
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
   } else if constexpr (PER == 4) {

@@ -4,6 +4,7 @@
 
 #include <math_constants.h>
 
+#include "checked.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 #include "schedule.cuh"

@@ -155,7 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
     it.valid = true;
     if constexpr (kMode == kModeJagged) {
       (void)i;
-      const int4 w = p.work_items[cl];  // 256 rows of one sequence
+      // 256 rows of one sequence (cl < the item count: see the early return above)
+      const int4 w = check_index(cl, *p.work_count, &g_prefill_status) ? p.work_items[cl] : make_int4(0, 0, 0, 0);
       it.b = 0;
       it.h = blockIdx.y;
       it.u_lo = w.z;
@@ -252,6 +253,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
+      // a tile load whose coordinates fail the checked build's test loads tile
+      // (0, 0, 0, 0) instead, so the pipeline's barriers still complete
+      auto load = [&](void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2, int c3, int heads,
+                      int rows) {
+        if (!check_tile(c0, c1, c2, c3, D, heads, rows, p.B, 256, &g_prefill_status)) c0 = c1 = c2 = c3 = 0;
+        tma_load_4d_pair(dst, map, bar, c0, c1, c2, c3);
+      };
       int filled[2] = {0, 0};  // tiles issued into the K ring and the V ring
       int q_loads = 0;
       bool ok = true;
@@ -271,11 +279,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
         if (ring == 0) {
           // K: this CTA's 64 keys of the tile, all 256 columns
           for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_4d_pair(dst + blk * C::K_BLOCK, &mk, full0, blk * 64, hk, kstart + C::KH * (int)rank, bb);
+            load(dst + blk * C::K_BLOCK, &mk, full0, blk * 64, hk, kstart + C::KH * (int)rank, bb, p.h_kv, p.S_kv);
         } else {
           // V: the tile's 128 keys, this CTA's 64 columns of each 128-column half
           for (int hs = 0; hs < C::NH; ++hs)
-            tma_load_4d_pair(dst + hs * C::V_BLOCK, &mv, full0, hs * C::SC + C::VH * (int)rank, hk, kstart, bb);
+            load(dst + hs * C::V_BLOCK, &mv, full0, hs * C::SC + C::VH * (int)rank, hk, kstart, bb, p.h_kv, p.S_kv);
         }
         ++fills;
         return true;
@@ -296,7 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
         if (rank == 0) mbar_arrive_expect_tx(&bar_q, 2 * C::Q_BYTES);
         const uint32_t q0 = mapa_shared(&bar_q, 0);
         for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d_pair(sQ + blk * C::Q_BLOCK, &mq, q0, blk * 64, it.h, it.q_lo, it.b);
+          load(sQ + blk * C::Q_BLOCK, &mq, q0, blk * 64, it.h, it.q_lo, it.b, p.h_q, p.S_q);
         ++q_loads;
         TileWalk kw = walk, vw = walk;
         int ch, st, me;
@@ -624,9 +632,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
         lr_run += xch_lr[ep][(kq + o) % C::WPR][row];
       }
       if (ok) {
-        const bool row_valid = q_row < q_hi;
         const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
         const size_t lse_idx = ((size_t)b * p.h_q + h) * p.S_q + q_row;
+        const long long rows_all = (long long)p.B * p.S_q * p.h_q;
+        const bool row_valid = q_row < q_hi && check_index((long long)row_idx, rows_all, &g_prefill_status) &&
+                               check_index((long long)lse_idx, rows_all, &g_prefill_status);
         constexpr float kLn2 = 0.693147180559945309f;
         if constexpr (kMode != kModePartial) {
           const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;

@@ -97,7 +97,7 @@ struct PairUnit {
 template <int kMode>
 __device__ __forceinline__ PairUnit pair_unit(const PrefillParams& p, int k) {
   if constexpr (kMode == kModeJagged) {
-    const int2 u = p.work_units[k / p.h_q];
+    const int2 u = check_index(k / p.h_q, p.work_count[1], &g_prefill_status) ? p.work_units[k / p.h_q] : make_int2(0, 0);
     const int n = min(u.y, *p.work_count - u.x);
     return PairUnit{u.x, n > 0 ? n : 0, k % p.h_q};
   } else {
@@ -114,7 +114,8 @@ __device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int k, int
   constexpr int BM = 128;
   PairItem it;
   if constexpr (kMode == kModeJagged) {
-    const int4 w = p.work_items[k];  // a 256-row Q tile of one sequence
+    // a 256-row Q tile of one sequence (a failed check reads an empty item)
+    const int4 w = check_index(k, *p.work_count, &g_prefill_status) ? p.work_items[k] : make_int4(0, 0, 0, 0);
     const int a_hi = w.z + min(w.w, BM);
     it.b = 0;
     it.st0 = SubTile{h, w.z, a_hi};
@@ -257,6 +258,13 @@ __global__ void __launch_bounds__(352, 1)
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
+      // a tile load whose coordinates fail the checked build's test loads tile
+      // (0, 0, 0, 0) instead, so the pipeline's barriers still complete
+      auto load = [&](void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2, int c3, int heads,
+                      int rows) {
+        if (!check_tile(c0, c1, c2, c3, D, heads, rows, p.B, 256, &g_prefill_status)) c0 = c1 = c2 = c3 = 0;
+        tma_load_4d(dst, map, bar, c0, c1, c2, c3);
+      };
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;   // K/V slabs issued so far (all items)
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(352, 1)
         uint8_t* dst = sKV + stage * C::SLAB_BYTES;
         mbar_arrive_expect_tx(&bar_full[stage], C::SLAB_BYTES);
         for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], blk * 64, hk, start, b);
+          load(dst + blk * C::BLOCK_BYTES, map, &bar_full[stage], blk * 64, hk, start, b, p.h_kv, p.S_kv);
         ++issued;
         if (++stage == C::NST) {
           stage = 0;
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(352, 1)
           for (int x = 0; x < nq; ++x) {
             const SubTile t = x ? it.st1 : it.st0;
             for (int blk = 0; blk < D / 64; ++blk)
-              tma_load_4d(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, t.h, t.q_lo, it.b);
+              load(sQ + x * C::Q_BYTES + blk * C::BLOCK_BYTES, &mq, &bar_q, blk * 64, t.h, t.q_lo, it.b, p.h_q, p.S_q);
           }
           ++q_loads;
           walk_next(kw, s0, me);
@@ -587,9 +595,11 @@ __global__ void __launch_bounds__(352, 1)
           }
           tc_fence_after_sync();
         }
-        const bool row_valid = q_row < me_t.q_hi;
         const size_t row_idx = ((size_t)it.b * p.S_q + q_row) * p.h_q + me_t.h;
         const size_t lse_idx = ((size_t)it.b * p.h_q + me_t.h) * p.S_q + q_row;
+        const long long rows_all = (long long)p.B * p.S_q * p.h_q;
+        const bool row_valid = q_row < me_t.q_hi && check_index((long long)row_idx, rows_all, &g_prefill_status) &&
+                               check_index((long long)lse_idx, rows_all, &g_prefill_status);
         constexpr float kLn2 = 0.693147180559945309f;
         if constexpr (kMode != kModePartial) {
           const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;

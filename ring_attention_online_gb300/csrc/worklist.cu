@@ -25,6 +25,7 @@
 //
 // Output buffer: int item count at word 0, int unit count at word 1, items
 // from byte 16 (max_items of them), then the units.
+#include "checked.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -102,7 +103,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
             items[pos] = make_int4(begin, len, tile_start, extent);
           }
         }
-        units[ubase + uexcl] = make_int2(base + excl, nt);  // ubase + uexcl < num_seqs
+        if (check_index((long long)ubase + uexcl, num_seqs, &g_worklist_status))  // < num_seqs by construction
+          units[ubase + uexcl] = make_int2(base + excl, nt);
       }
       __syncthreads();
       if (tid == 0) {
@@ -136,6 +138,18 @@ __global__ void selftest_timeout_kernel(uint64_t timeout_ns) {
   fence_barrier_init();
   mbar_wait_bounded(&bar, 0, &abort_flag, &g_worklist_status, kStatusTimeout | (0xA0u << kStatusSiteShift),
                     timeout_ns);
+}
+
+// Index 1 of a one-element buffer, through the checked build's store check: a
+// checked build reports it (kStatusBounds) and skips the store; without checks
+// the store goes to index 0, in range either way.
+__global__ void selftest_bounds_kernel(int* buf) {
+  if (check_index(1, 1, &g_worklist_status)) buf[0] = 1;
+}
+
+attn_status_t launch_selftest_bounds(int* buf, cudaStream_t s) {
+  selftest_bounds_kernel<<<1, 1, 0, s>>>(buf);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t s) {

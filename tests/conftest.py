@@ -18,3 +18,13 @@ def golden():
     import json
     with open(os.path.join(ROOT, "tests", "golden", "worked_examples.json")) as f:
         return json.load(f)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _library_variant():
+    """With ATTN_LIBRARY=checked every test runs on the checked debug build: make sure
+    that is the library that loaded."""
+    if os.environ.get("ATTN_LIBRARY") == "checked":
+        import ring_attention_online_gb300 as ra
+        assert ra.attn_build_checked(), "ATTN_LIBRARY=checked loaded a library without checks"
+    yield
