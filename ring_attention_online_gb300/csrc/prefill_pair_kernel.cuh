@@ -63,6 +63,19 @@ struct PairCfg {
   static constexpr int THREADS = 352;
   static_assert(D == 64 || D == 128, "paired kernel: head dim 64 or 128");
   static_assert(NST >= 3, "K(j+1) must be loadable while K(j) and V(j) are held");
+  // One ring holds K and V.  The producer pushes, over all items, K0 V0 K1 V1
+  // ... (each item pushes 2n slabs starting with K), so slab s is a K tile iff s
+  // is even and lives in stage s % NST, round s / NST.  Before an issuer waits
+  // for slab s, the stage's previous fill, slab s - NST, must be complete: a
+  // parity wait cannot tell it from slab s (the phase before the awaited one
+  // reads as complete).  With NST even, slab s - NST is of the same kind and
+  // the same issuer waited for it earlier.  With NST odd (head dim 128: 5) it
+  // belongs to the other issuer, and the order of the waits is what excludes
+  // the hazard (see ORDER at the two wait sites); checked builds verify it at
+  // run time.  Split K and V rings would exclude it structurally, but measured
+  // 1.2 % (ring), 2.3-3.6 % (sliding window) and up to 2.2 % (jagged) slower
+  // with either split of the five stages.
+  static_assert(NST % 2 == 0 || NST >= 5, "the ordering argument for an odd ring needs five stages or more");
   static_assert(SMEM_BYTES <= 227 * 1024 - 512, "shared memory budget");
 };
 
@@ -184,6 +197,11 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
+#if ATTN_CHECKED
+  // rounds of each stage whose fill its issuer has observed complete
+  __shared__ int ring_seen[C::NST];
+  if (threadIdx.x < C::NST) ring_seen[threadIdx.x] = 0;
+#endif
 
   const int total = pair_item_count<kMode>(p);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,10 +369,28 @@ __global__ void __launch_bounds__(352, 1)
       int q_items = 0;         // items whose Q was consumed
       bool ok = true;
       // slab s (push order K0 V0 K1 V1 ... over all items) lives in stage
-      // s % NST, phase (s / NST) & 1
+      // s % NST, phase (s / NST) & 1.
+      // ORDER: the stage's previous fill, slab s - NST, is complete before this
+      // wait.  With NST odd it is the other issuer's: for K slab 2m the S issuer
+      // has, before this wait, waited for the previous P.V of a sub-tile active
+      // on the K tile before, which the P.V issuer issued after waiting for V
+      // slab 2(m - (NST + 1) / 2) + 1 = s - NST; for V slab 2m + 1 the P.V
+      // issuer has waited for P of the tile before, which its softmax computed
+      // from an S MMA issued after the S issuer waited for K slab
+      // 2(m - (NST - 1) / 2) = s - NST.  Checked builds verify it (the stage's
+      // previous round observed by its issuer) and report a violation as
+      // ATTN_ERR_BOUNDS.
       auto wait_slab = [&](int s) -> bool {
+#if ATTN_CHECKED
+        if (*reinterpret_cast<volatile int*>(&ring_seen[s % C::NST]) < s / C::NST)
+          atomicOr(&g_prefill_status, kStatusBounds);
+#endif
         if (!pf_wait(&bar_full[s % C::NST], (uint32_t)((s / C::NST) & 1), &abort_flag, 2)) return false;
         tc_fence_after_sync();
+#if ATTN_CHECKED
+        *reinterpret_cast<volatile int*>(&ring_seen[s % C::NST]) = s / C::NST + 1;
+        __threadfence_block();
+#endif
         return true;
       };
       for (int r = 0; ok && (kPersistent || r == 0); ++r) {
