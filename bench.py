@@ -310,6 +310,49 @@ def make_workload(name: str, device, batch=None, seq=None):
     return w
 
 
+def host_link(device, nbytes: int = 256 << 20, reps: int = 5):
+    """Pinned host <-> device copy bandwidth (one cudaMemcpyAsync per copy), each
+    direction alone and both at once on two streams, best of `reps`, with the
+    host's NUMA layout: the ceiling of the end-to-end step."""
+    import torch
+    h = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    d = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    s = [torch.cuda.Stream(device) for _ in range(2)]
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps + 1):  # the first run warms up
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(device)
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s[0]):
+            d[0].copy_(h[0], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s[1]):
+            h[1].copy_(d[1], non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+    try:
+        nodes = open("/sys/devices/system/node/online").read().strip()
+    except OSError:
+        nodes = "unknown"
+    cpus = sorted(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else []
+    return {"h2d_gbs": round(nbytes / t_in / 1e9, 1), "d2h_gbs": round(nbytes / t_out / 1e9, 1),
+            "both_gbs": round(2 * nbytes / t_both / 1e9, 1), "numa_nodes_online": nodes,
+            "process_cpus": f"{cpus[0]}-{cpus[-1]} ({len(cpus)})" if cpus else "unknown",
+            "how": "pinned torch tensors, one cudaMemcpyAsync per copy, 256 MiB, best of 5"}
+
+
 def time_steps(step, K: int, W: int, device):
     import torch
     stream = torch.cuda.current_stream(device)
@@ -484,6 +527,15 @@ def run_ours(args):
         line["e2e"] = {"value": round(units_e2e / (ms_e2e_max / 1e3), 2), "unit": w["unit"],
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2,
                        "gpu_launches": e2e_launches}
+        # the step's copies can take no less than the link allows: all inputs in one
+        # direction, all outputs in the other, and both together on the shared link
+        link = host_link(device)
+        floor_ms = 1e3 * max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                             (h2d + d2h) / (link["both_gbs"] * 1e9))
+        link["step_floor_ms"] = round(floor_ms, 3)
+        link["e2e_ms_per_step"] = round(ms_e2e_max / K2, 3)
+        link["e2e_frac_of_link_floor"] = round(floor_ms / (ms_e2e_max / K2), 3)
+        line["e2e"]["host_link"] = link
         line["gpu_launches"] += e2e_launches
         del host_in, host_out
     del w
