@@ -84,8 +84,8 @@ dim3 persistent_pair_grid(long long units) {
 }
 
 // Fills the work-item decomposition of the paired kernel and its grid (one
-// item per CTA); the single-tile kernel runs one CTA per SM over units of two
-// Q tiles of one (batch, head).  False when the item count does not fit a
+// item per CTA); the head-dim-256 kernel runs one CTA pair per two SMs over
+// units of up to two 256-row pair items of one (batch, head or head pair).  False when the item count does not fit a
 // 32-bit item index.
 bool dense_grid(PrefillParams& p, int D, dim3* grid) {
   if (!paired(D)) {

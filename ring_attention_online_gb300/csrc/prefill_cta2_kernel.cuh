@@ -2,7 +2,7 @@
 // pairs: tcgen05 with cta_group::2, 256 query rows per pair sharing every K/V
 // tile.
 //
-// What it computes, by source (the same as the paired and single-tile kernels):
+// What it computes, by source (the same as the paired kernel of head dims 64/128):
 //  * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel: per KV block,
 //    scores = Q.K^T, m = rowmax, exp(scores - m), l = rowsum, O = exp . V,
 //    merged into the running (m, l, O) with m_new = max(m, m_step) and the
@@ -46,9 +46,9 @@
 //   warp 1      TMEM owner; rank 0: S issuer, S(j) = Q.K_j^T for the pair.
 //   warp 10     rank 0: P.V issuer.  rank 1: idle.
 //   warps 2..9  softmax + epilogue of this CTA's 128 rows, two warps per row (a
-//               half of the tile's keys and of O's columns each), exactly as in
-//               the single-tile kernel; their "S read" and "P written" signals
-//               go to rank 0's barriers (one arrival per warp).
+//               half of the tile's keys and of O's columns each, the pair of
+//               warps exchanging row maxima once per tile); their "S read" and
+//               "P written" signals go to rank 0's barriers (one arrival per warp).
 // Every MMA commit is multicast to both CTAs' barriers.  Every wait is bounded:
 // a timeout sets the library's device status, the CTA skips its remaining
 // work, waits for its copies in flight (rank 0 on its barriers; rank 1, whose

@@ -1,7 +1,7 @@
 // Blockwise online-softmax attention forward for head dimensions 64 and 128:
 // two 128-row Q sub-tiles per CTA that share every K/V tile.
 //
-// What it computes is the same as the single-tile kernel (prefill_kernel.cuh):
+// What it computes is the same as the head-dim-256 kernel (prefill_cta2_kernel.cuh):
 // per KV tile, S = Q.K^T, the running (m, l, O) updated by online softmax
 // ("kernbench2 _gqa_prefill_long.py", step 0 partial and the ring-step merge),
 // O / l at the end, over the tiles of a ring-order walk that stops at

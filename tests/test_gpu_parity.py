@@ -118,13 +118,44 @@ def test_prefill_window_ring_chunks_of_whole_tiles(window):
     close_lse(lse, L)
 
 
+@pytest.mark.parametrize("C", [2, 3])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("h_q,h_kv", [(3, 3), (4, 2)])
+def test_prefill_ring_d256_cta_pairs(C, causal, h_q, h_kv):
+    """Head dim 256 (CTA pairs) with a ring walk over C chunks of 347 and 232 keys, not
+    whole tiles: Q-tile pairs (MHA, the odd tile count leaves rank 1 an empty tile) and
+    head pairs (even GQA group), causal and full."""
+    B, S_, D = 2, 694, 256
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=120 + C + h_q)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill(q, k, v, o, lse, causal=causal, num_chunks=C)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), causal)
+    close_o(o, O, f"attn_prefill D=256 ring C={C} causal={causal} heads {h_q}/{h_kv}")
+    close_lse(lse, L)
+
+
+@pytest.mark.parametrize("window", [100, 300])
+def test_prefill_window_ring_d256_cta_pairs(window):
+    """Head dim 256 sliding window over a three-chunk ring (a pair's rows at the lower
+    window edge see fewer tiles than the pair walks)."""
+    B, S_, h_q, h_kv, D = 1, 900, 4, 4, 256
+    q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "fp16", seed=130 + window)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
+    ra.attn_prefill_window(q, k, v, o, lse, window=window, num_chunks=3)
+    O, L = A.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(D), True, window=window)
+    close_o(o, O, f"attn_prefill_window D=256 ring w={window}")
+    close_lse(lse, L)
+
+
 # ---------------------------------------------------------------------- sliding window
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("window", [0, 1, 100, 127, 128, 129, 300, 5000])
 @pytest.mark.parametrize("h_q,h_kv", [(4, 2), (2, 2)])
 def test_prefill_window_parity(D, window, h_q, h_kv, dtype):
-    """Both kernels (paired for 64/128 with head pairs and Q-tile pairs, single-tile for
+    """Both kernels (paired for 64/128 with head pairs and Q-tile pairs, CTA pairs for
     256): the walk floor, the per-row lower mask and sub-tiles sitting out tiles below
     their window; window 5000 > S is plain causal."""
     B, S_ = 1, 650
@@ -153,14 +184,16 @@ def test_prefill_window_ring_gqa(C):
 # ---------------------------------------------------------------------- persistent grids
 @pytest.mark.parametrize("causal", [True, False])
 def test_prefill_d256_persistent_many_units(causal):
-    """Head dim 256 runs one CTA per SM over units of two Q tiles: here there are more
-    than twice as many units as SMs, so every CTA chains several, and the odd Q-tile
-    count gives every (batch, head) a unit with an empty second slot (the causal middle
-    tile, the non-causal last one)."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    """Head dim 256 runs one CTA pair per two SMs over units of two 256-row pair items;
+    with an even group size (48 / 8 = 6) an item is one Q tile of two query heads.  Here
+    there are more than twice as many units as pairs, so every pair chains several, and
+    the odd Q-tile count gives every (batch, head pair) a unit with an empty second slot
+    (the causal middle tile, the non-causal last one)."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
     B, S_, h_q, h_kv, D = 4, 300, 48, 8, 256
-    units = B * h_q * (((S_ + 127) // 128 + 1) // 2)
-    assert units > 2 * sms
+    n_it = (S_ + 127) // 128  # pair items per (batch, head pair)
+    units = B * (h_q // 2) * ((n_it + 1) // 2)
+    assert units > 2 * pairs
     q, k, v = gen((B, S_, h_q, D), (B, S_, h_kv, D), "bf16", seed=60 + causal)
     o = torch.empty_like(q)
     lse = torch.empty(B, h_q, S_, device="cuda", dtype=torch.float32)
@@ -281,13 +314,14 @@ def test_partial_causal_positions_and_identity(D, dtype):
 
 
 def test_partial_d256_persistent_many_units():
-    """Partials at head dim 256 run on the persistent grid: more two-tile units than
-    SMs, GQA, causal positions that leave some Q tiles fully visible, some partly and
-    some (the earliest rows) with no visible key at all, so that empty items and
-    identity rows sit between full ones in a CTA's sequence of units."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    """Partials at head dim 256 run on the persistent grid of CTA pairs: more units
+    than pairs, GQA (head-pair items), causal positions that leave some Q tiles fully
+    visible, some partly and some (the earliest rows) with no visible key at all, so
+    that empty items and identity rows sit between full ones in a pair's sequence of
+    units."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
     B, S_q, S_kv, h_q, h_kv, D = 3, 520, 900, 48, 8, 256
-    assert B * h_q * (((S_q + 127) // 128 + 1) // 2) > sms
+    assert B * (h_q // 2) * (((S_q + 127) // 128 + 1) // 2) > pairs
     q, k, v = gen((B, S_q, h_q, D), (B, S_kv, h_kv, D), "bf16", seed=81)
     scale = 1 / math.sqrt(D)
     m = torch.empty(B, h_q, S_q, device="cuda")
