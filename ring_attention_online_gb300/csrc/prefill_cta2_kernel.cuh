@@ -1,6 +1,6 @@
-// Blockwise online-softmax attention forward for head dimension 256 on CTA
-// pairs: tcgen05 with cta_group::2, 256 query rows per pair sharing every K/V
-// tile.
+// Blockwise online-softmax attention forward on CTA pairs (head dimension 256;
+// the template also takes 128): tcgen05 with cta_group::2, 256 query rows per
+// pair sharing every K/V tile.
 //
 // What it computes, by source (the same as the paired kernel of head dims 64/128):
 //  * "kernbench2 _gqa_prefill_long.py", gqa_prefill_long_kernel: per KV block,
@@ -36,7 +36,7 @@
 // same length (items x and n - 1 - x), the longer first.  A jagged cluster
 // takes one worklist item of 256 rows.
 //
-// CTA layout (352 threads; both CTAs of the pair run the same roles except
+// CTA layout (480 threads; both CTAs of the pair run the same roles except
 // where noted):
 //   warp 0      TMA producer: this CTA's Q tile, then its halves of the K and V
 //               tiles through a K ring and a V ring of shared-memory stages.
@@ -45,10 +45,16 @@
 //               so one wait tells an issuer that both halves have landed.
 //   warp 1      TMEM owner; rank 0: S issuer, S(j) = Q.K_j^T for the pair.
 //   warp 10     rank 0: P.V issuer.  rank 1: idle.
-//   warps 2..9  softmax + epilogue of this CTA's 128 rows, two warps per row (a
-//               half of the tile's keys and of O's columns each, the pair of
-//               warps exchanging row maxima once per tile); their "S read" and
-//               "P written" signals go to rank 0's barriers (one arrival per warp).
+//   warps 2..9  softmax of this CTA's 128 rows, two warps per row (a half of
+//               the tile's keys and of O's columns each, the pair of warps
+//               exchanging row maxima once per tile); their "S read" and "P
+//               written" signals go to rank 0's barriers (one arrival per warp).
+//               At the end of an item they leave each row's (m, l) in shared
+//               memory and go on to the next item.
+//   warps 11..14 epilogue of this CTA's 128 rows, one warp per TMEM lane
+//               quarter: once the item's last P.V is done they read O out of
+//               TMEM, signal "O free" to rank 0 (the next item's first P.V
+//               waits for it) and store O / l and the LSE.
 // Every MMA commit is multicast to both CTAs' barriers.  Every wait is bounded:
 // a timeout sets the library's device status, the CTA skips its remaining
 // work, waits for its copies in flight (rank 0 on its barriers; rank 1, whose
@@ -64,8 +70,9 @@
 
 namespace attn {
 
+template <int D_>
 struct Cta2Cfg {
-  static constexpr int D = 256;
+  static constexpr int D = D_;
   static constexpr int BM = 128;                // query rows per CTA (256 per pair)
   static constexpr int BN = 128;                // keys per KV tile
   static constexpr int SC = 128;                // columns of D per P.V MMA (a half of D)
@@ -75,15 +82,17 @@ struct Cta2Cfg {
   static constexpr int Q_BLOCK = 128 * 128;     // Q: 128 rows x 64 columns (128 B, swizzled)
   static constexpr int K_BLOCK = KH * 128;      // K half: 64 keys x 64 columns
   static constexpr int V_BLOCK = BN * 128;      // V: 128 keys x 64 columns
-  static constexpr int Q_BYTES = BM * D * 2;    // 64 KB
+  static constexpr int Q_BYTES = BM * D * 2;    // 64 KB at head dim 256
   // one stage per K or V tile: this CTA's 64 keys x 256 columns of K, or the
   // tile's 128 keys x this CTA's 2 x 64 columns of V (one 64-column block per
   // 128-column half of D).  One barrier per tile: each wait of an MMA issuer
   // costs the tensor pipe a bubble (the wait holds the issuing thread until its
   // MMAs drain), and with one wait per slab (two per tile) the kernel ran
   // 1428-1510 vs 1471-1558 TFLOP/s on dense causal B=8 H=32 S=4096.
-  static constexpr int STAGE_BYTES = 32768;
-  static constexpr int RING = 2;                // stages per ring: two tiles of K, two of V
+  static constexpr int STAGE_BYTES = KH * D * 2;
+  // stages per ring (K tiles; V tiles): as many as fit next to Q and the static
+  // part (2 at head dim 256, 5 at 128)
+  static constexpr int RING = (213 * 1024 - Q_BYTES) / (2 * STAGE_BYTES);
   static constexpr int NST = 2 * RING;
   static constexpr int SMEM_BYTES = Q_BYTES + NST * STAGE_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -98,22 +107,28 @@ struct Cta2Cfg {
   static constexpr int KW = BN / WPR;           // keys of a tile per softmax warp
   static constexpr int OW = D / WPR;            // O columns per softmax warp
   static constexpr int PV_WARP = 2 + SM_WARPS;  // the P.V issuer's warp (rank 0)
-  static constexpr int THREADS = 32 * (3 + SM_WARPS);
+  static constexpr int EPI_WARP = 3 + SM_WARPS;  // first of the four epilogue warps
+  static constexpr int THREADS = 32 * (EPI_WARP + 4);
+  // 15 warps put four on three of the four SM sub-partitions (16K registers
+  // each), so at most 128 registers per thread
+  static constexpr int MAX_THREADS = 512;
   static constexpr uint16_t kBoth = 3;          // multicast mask of a commit: both CTAs
   static constexpr uint64_t kPeerCopyDrainNs = 200000;  // rank 1's wait for its copies after an abort
   static constexpr uint32_t kSignals = 2 * SM_WARPS;  // arrivals per phase: every softmax warp of the pair
+  static constexpr uint32_t kEpiSignals = 2 * 4;       // "O free": every epilogue warp of the pair
   static_assert(WPR == 2 || WPR == 4, "softmax warps per row");
-  static_assert(KH * D * 2 == STAGE_BYTES && BN * VH * 2 * NH == STAGE_BYTES, "stage size");
+  static_assert(D == 128 || D == 256, "CTA-pair kernel: head dim 128 or 256");
+  static_assert(BN * VH * 2 * NH == STAGE_BYTES, "a K and a V stage are the same size");
+  static_assert(RING >= 2, "K(j+1) must be loadable while K(j) is read");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES + 13 * 1024 <= 227 * 1024, "shared memory budget (static part < 13 KB)");
 };
 
-template <bool kBf16, int kMode, bool kOneChunk>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
+template <int D, bool kBf16, int kMode, bool kOneChunk>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THREADS, 1)
     prefill_cta2_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const PrefillParams p) {
-  using C = Cta2Cfg;
-  constexpr int D = C::D;
+  using C = Cta2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_qe, bar_fin, bar_exit;
   __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2] (both CTAs)
@@ -122,10 +137,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
   __shared__ uint64_t bar_sfree[2];  // the pair's softmax warps have read S(j) out of TMEM (j % 2)
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
-  __shared__ float xch_max[2][C::WPR][128];                       // [tile parity][key part][row]
-  __shared__ float xch_l[2][C::WPR][128], xch_lr[2][C::WPR][128];  // [item parity][key part][row]
+  __shared__ float xch_max[2][C::WPR][128];  // [tile parity][key part][row]
   __shared__ uint64_t bar_x[2][4];  // exchange of a row's warps: [tile parity][lane quarter]
-  __shared__ uint64_t bar_xe[4];                         // end-of-row exchange per lane quarter
+  // a finished item's row state, from the softmax warps to the epilogue warps:
+  // [item parity][row] and [item parity][key part][row]
+  __shared__ float ep_m[2][128], ep_mmax[2][128];
+  __shared__ float ep_l[2][C::WPR][128], ep_lr[2][C::WPR][128];
+  __shared__ uint64_t bar_ep_full[2], bar_ep_empty[2];  // [item parity]
+  __shared__ uint64_t bar_ofree;  // rank 0: the epilogue warps of both CTAs have read O
 
   const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs of the pair
   const int cl = (int)(blockIdx.x >> 1);
@@ -232,8 +251,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
       mbar_init(&bar_sfree[i], C::kSignals);
       mbar_init(&bar_p[i], C::kSignals);
       for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 32 * C::WPR);
+      mbar_init(&bar_ep_full[i], 32 * C::SM_WARPS);
+      mbar_init(&bar_ep_empty[i], 32 * 4);
     }
-    for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_xe[q4], 32 * C::WPR);
+    mbar_init(&bar_ofree, C::kEpiSignals);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -370,6 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
       int g = 0;          // S (or PV) groups issued so far, all items: barrier phases
       int tile_base = 0;  // tiles of this issuer's ring taken by the earlier items
       int q_used = 0;     // Q tiles consumed (S issuer)
+      int o_items = 0;    // items whose P.V MMAs were issued (P.V issuer)
       for (int i = 0; ok && i < n_my; ++i) {
         const Item it = get_item(i);
         if (!it.valid) continue;
@@ -409,6 +431,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
           // the item's S MMAs, the last readers of its Q, release both Q buffers
           if (ok) mma_commit_cta2(&bar_qe, C::kBoth);
         } else {
+          // the item's first P.V starts O afresh: the epilogue warps of both CTAs
+          // have read the previous item's O out of TMEM
+          if (o_items > 0) {
+            ok = pf_wait_outlined(&bar_ofree, (uint32_t)((o_items - 1) & 1), &abort_flag, 14);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          ++o_items;
           for (int j = 0; ok && j < n; ++j, ++g) {
             ok = pf_wait_outlined(&bar_p[g & 1], (uint32_t)((g >> 1) & 1), &abort_flag, 3);
             if (!ok) break;
@@ -441,7 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
       pf_drain(&bar_fin, 0);
     }
   } else if (warp >= 2 && warp < 2 + C::SM_WARPS) {
-    // ========================================================== softmax + epilogue (both CTAs)
+    // ========================================================== softmax (both CTAs)
     // WPR warps share each TMEM lane quarter: warp 2 + 4 kq + (wq - 2) mod 4 ...
     // takes key part kq of every row of lane quarter wq (keys [KW kq, KW kq + KW)
     // of a tile, O columns [OW kq, OW kq + OW)).  The row's warps exchange their
@@ -471,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
       if (!it.valid) continue;
       TileWalk sw_walk;
       const int n = item_walk(it, sw_walk);
-      const int b = it.b, h = it.h, q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
+      const int q_lo = it.q_lo, q_hi = it.q_hi, q_pos0 = it.q_pos0, kv_pos0 = it.kv_pos0;
       const int q_row = q_lo + row;
       float m_run = -CUDART_INF_F;   // reference max (exp2 domain), raised lazily
       float l_run = 0.f;             // this part's sum of exp2(x - m_run) in fp32: l and LSE
@@ -614,93 +644,151 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
         if (lane == 0) signal(&bar_p[buf], p_remote[buf]);
       }
       if (ok && n > 0) {
-        // the item's last P.V (the earlier ones are done or finish before it)
-        ok = pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8);
+        // hand the row's state to the epilogue warps (one buffer per item
+        // parity: before a buffer is reused, the epilogue warps have read what
+        // the item two back left in it)
+        const int eb = n_ep & 1;
+        if (n_ep >= 2) ok = pf_wait_outlined(&bar_ep_empty[eb], (uint32_t)(((n_ep >> 1) - 1) & 1), &abort_flag, 15);
+        if (ok) {
+          ep_l[eb][kq][row] = l_run;
+          ep_lr[eb][kq][row] = lr_run;
+          if (kq == 0) {
+            ep_m[eb][row] = m_run;
+            ep_mmax[eb][row] = m_max;
+          }
+          mbar_arrive(&bar_ep_full[eb]);
+        }
+        ++n_ep;
+      }
+    }  // items
+  } else if (warp >= C::EPI_WARP) {
+    // ========================================================== epilogue (both CTAs)
+    // One warp per TMEM lane quarter (warp w takes the rows of quarter w mod 4,
+    // one row per thread).  Per item with tiles: the row's state from the
+    // softmax warps, then, once the item's last P.V is done, O out of TMEM,
+    // after which the P.V issuer may start the next item's O while these warps
+    // normalise and store this one.  The softmax warps meanwhile already work
+    // on the next item, so an item boundary costs them no epilogue.
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t ofree_remote = mapa_shared(&bar_ofree, 0);
+    const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+    constexpr float kLn2 = 0.693147180559945309f;
+    bool ok = true;
+    int gj = 0;    // tiles so far, all items
+    int n_ep = 0;  // items with tiles so far
+    for (int i = 0; ok && i < n_my; ++i) {
+      const Item it = get_item(i);
+      if (!it.valid) continue;
+      TileWalk ep_walk;
+      const int n = item_walk(it, ep_walk);
+      float m_run = -CUDART_INF_F, l_run = 0.f, lr_run = 0.f, m_max = -CUDART_INF_F;
+      if (n > 0) {
+        const int eb = n_ep & 1;
+        if (!pf_wait_outlined(&bar_ep_full[eb], (uint32_t)((n_ep >> 1) & 1), &abort_flag, 16)) {
+          ok = false;
+          break;
+        }
+        m_run = ep_m[eb][row];
+        m_max = ep_mmax[eb][row];
+#pragma unroll
+        for (int o = 0; o < C::WPR; ++o) {
+          l_run += ep_l[eb][o][row];
+          lr_run += ep_lr[eb][o][row];
+        }
+        mbar_arrive(&bar_ep_empty[eb]);
+        ++n_ep;
+        gj += n;
+        // the item's last P.V (the earlier ones finish before it)
+        if (!pf_wait_outlined(&bar_o[(gj - 1) & 1], (uint32_t)(((gj - 1) >> 1) & 1), &abort_flag, 8)) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
       }
-      // the row's sums are split over its parts (one exchange buffer per item
-      // parity: a part cannot get two epilogues ahead of the others)
-      const int ep = n_ep & 1;
-      xch_l[ep][kq][row] = l_run;
-      xch_lr[ep][kq][row] = lr_run;
-      mbar_arrive(&bar_xe[wq]);
-      if (ok) ok = pf_wait_outlined(&bar_xe[wq], (uint32_t)ep, &abort_flag, 10);
-      ++n_ep;
-#pragma unroll
-      for (int o = 1; o < C::WPR; ++o) {
-        l_run += xch_l[ep][(kq + o) % C::WPR][row];
-        lr_run += xch_lr[ep][(kq + o) % C::WPR][row];
-      }
-      if (ok) {
-        const size_t row_idx = ((size_t)b * p.S_q + q_row) * p.h_q + h;
-        const size_t lse_idx = ((size_t)b * p.h_q + h) * p.S_q + q_row;
-        const long long rows_all = (long long)p.B * p.S_q * p.h_q;
-        const bool row_valid = q_row < q_hi && check_index((long long)row_idx, rows_all, &g_prefill_status) &&
-                               check_index((long long)lse_idx, rows_all, &g_prefill_status);
-        constexpr float kLn2 = 0.693147180559945309f;
+      const int q_row = it.q_lo + row;
+      const size_t row_idx = ((size_t)it.b * p.S_q + q_row) * p.h_q + it.h;
+      const size_t lse_idx = ((size_t)it.b * p.h_q + it.h) * p.S_q + q_row;
+      const long long rows_all = (long long)p.B * p.S_q * p.h_q;
+      const bool row_valid = q_row < it.q_hi && check_index((long long)row_idx, rows_all, &g_prefill_status) &&
+                             check_index((long long)lse_idx, rows_all, &g_prefill_status);
+      // O / lr in the input type; a partial's fp32 O re-referenced to the true
+      // max and re-weighted so that O / l equals the consistently normalised
+      // O_acc / lr
+      const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
+      const float f = any ? fast_exp2(m_run - m_max) : 0.f;
+      float so;
+      if constexpr (kMode != kModePartial)
+        so = lr_run > 0.f ? 1.f / lr_run : 0.f;
+      else
+        so = any ? f * (l_run / lr_run) : 0.f;
+      auto emit = [&](int cc, const uint32_t(&o)[32]) {
+        if (!row_valid) return;
         if constexpr (kMode != kModePartial) {
-          const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
-          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + kq * OW;
-          const bool o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
-#pragma unroll 1
-          for (int cc = 0; cc < OW / 32; ++cc) {
-            uint32_t o[32];
-            if (n > 0) {
-              tmem_ld32(lane_addr + C::O_COL + kq * OW + cc * 32, o);
-              tmem_ld_wait(o);
-            } else {
+          uint32_t w[16];
 #pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = 0u;
-            }
-            uint32_t w[16];
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_half2<kBf16>(__uint_as_float(o[2 * k]) * so, __uint_as_float(o[2 * k + 1]) * so);
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D + cc * 32;
+          // a warp's store touches 32 rows: 32-byte pieces halve the requests
+          // of 16-byte ones (the output's base decides)
+          if (o_v8) {
+            st_global_v8(orow, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            st_global_v8(orow + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              w[k] = pack_half2<kBf16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-            if (row_valid) {
-              // a warp's store touches 32 rows: 32-byte pieces halve the requests
-              // of 16-byte ones (the output's base decides)
-              if (o_v8) {
-                st_global_v8(orow + cc * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-                st_global_v8(orow + cc * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                  dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-              }
-            }
+            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
           }
-          if (p.lse != nullptr && row_valid && kq == 0)
-            p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
         } else {
-          const bool any = l_run > 0.f && m_max != -CUDART_INF_F;
-          const float f = any ? fast_exp2(m_run - m_max) : 0.f;  // re-reference to the true max
-          // O re-weighted so that O / l equals the consistently normalised O_acc / lr
-          const float fo = any ? f * (l_run / lr_run) : 0.f;
-          float* orow = p.o_part + row_idx * D + kq * OW;
-#pragma unroll 1
-          for (int cc = 0; cc < OW / 32; ++cc) {
-            uint32_t o[32];
-            if (n > 0) {
-              tmem_ld32(lane_addr + C::O_COL + kq * OW + cc * 32, o);
-              tmem_ld_wait(o);
-            } else {
+          float4* dst = reinterpret_cast<float4*>(p.o_part + row_idx * D + cc * 32);
 #pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = 0u;
-            }
-            if (row_valid) {
-              float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
-#pragma unroll
-              for (int v4 = 0; v4 < 8; ++v4)
-                dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * fo, __uint_as_float(o[4 * v4 + 1]) * fo,
-                                      __uint_as_float(o[4 * v4 + 2]) * fo, __uint_as_float(o[4 * v4 + 3]) * fo);
-            }
-          }
-          if (row_valid && kq == 0) {
-            p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
-            p.l_out[lse_idx] = any ? l_run * f : 0.f;
-          }
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * so, __uint_as_float(o[4 * v4 + 1]) * so,
+                                  __uint_as_float(o[4 * v4 + 2]) * so, __uint_as_float(o[4 * v4 + 3]) * so);
         }
+      };
+      if (n > 0) {
+        // two chunks of 32 columns in flight: chunk c + 1 loads while chunk c
+        // is normalised and stored
+        uint32_t oa[32], ob[32];
+        tmem_ld32(lane_addr + C::O_COL, oa);
+        tmem_ld_wait(oa);
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; cc += 2) {
+          tmem_ld32(lane_addr + C::O_COL + (cc + 1) * 32, ob);
+          emit(cc, oa);
+          tmem_ld_wait(ob);
+          if (cc + 2 < D / 32) {
+            tmem_ld32(lane_addr + C::O_COL + (cc + 2) * 32, oa);
+          } else {
+            // all of O is read: the next item's first P.V may overwrite it
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0)
+                mbar_arrive(&bar_ofree);
+              else
+                mbar_arrive_remote(ofree_remote);
+            }
+          }
+          emit(cc + 1, ob);
+          if (cc + 2 < D / 32) tmem_ld_wait(oa);
+        }
+      } else {
+        // no visible key: O = 0 (and LSE = -inf)
+        uint32_t z[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) z[k] = 0u;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) emit(cc, z);
+      }
+      if constexpr (kMode != kModePartial) {
+        if (p.lse != nullptr && row_valid) p.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -CUDART_INF_F;
+      } else if (row_valid) {
+        p.m_out[lse_idx] = any ? m_max * kLn2 : -CUDART_INF_F;
+        p.l_out[lse_idx] = any ? l_run * f : 0.f;
       }
     }  // items
   }
@@ -722,11 +810,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg::THREADS, 1)
   }
 }
 
-template <bool kBf16, int kMode, bool kOneChunk>
+template <int D, bool kBf16, int kMode, bool kOneChunk>
 attn_status_t launch_cta2_variant(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
-  using C = Cta2Cfg;
-  auto kern = prefill_cta2_kernel<kBf16, kMode, kOneChunk>;
+  using C = Cta2Cfg<D>;
+  auto kern = prefill_cta2_kernel<D, kBf16, kMode, kOneChunk>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
   if (grid.x == 0 || grid.x % 2 != 0) return ATTN_ERR_INVALID_ARG;
@@ -736,29 +824,30 @@ attn_status_t launch_cta2_variant(const PrefillParams& p, const CUtensorMap& mq,
 
 // Dense and window launches with one chunk, and every partial and jagged
 // launch (always one KV range), take the single-chunk instantiations.
-template <bool kBf16>
+template <int D, bool kBf16>
 attn_status_t launch_cta2_typed(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                 const CUtensorMap& mv, int mode, dim3 grid, cudaStream_t s) {
   const bool one = p.num_chunks == 1;
   switch (mode) {
     case kModeDense:
-      return one ? launch_cta2_variant<kBf16, kModeDense, true>(p, mq, mk, mv, grid, s)
-                 : launch_cta2_variant<kBf16, kModeDense, false>(p, mq, mk, mv, grid, s);
+      return one ? launch_cta2_variant<D, kBf16, kModeDense, true>(p, mq, mk, mv, grid, s)
+                 : launch_cta2_variant<D, kBf16, kModeDense, false>(p, mq, mk, mv, grid, s);
     case kModeWindow:
-      return one ? launch_cta2_variant<kBf16, kModeWindow, true>(p, mq, mk, mv, grid, s)
-                 : launch_cta2_variant<kBf16, kModeWindow, false>(p, mq, mk, mv, grid, s);
+      return one ? launch_cta2_variant<D, kBf16, kModeWindow, true>(p, mq, mk, mv, grid, s)
+                 : launch_cta2_variant<D, kBf16, kModeWindow, false>(p, mq, mk, mv, grid, s);
     case kModePartial:
-      return one ? launch_cta2_variant<kBf16, kModePartial, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+      return one ? launch_cta2_variant<D, kBf16, kModePartial, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
     case kModeJagged:
-      return one ? launch_cta2_variant<kBf16, kModeJagged, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
+      return one ? launch_cta2_variant<D, kBf16, kModeJagged, true>(p, mq, mk, mv, grid, s) : ATTN_ERR_INVALID_ARG;
   }
   return ATTN_ERR_INVALID_ARG;
 }
 
-inline attn_status_t launch_cta2_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+template <int D>
+attn_status_t launch_cta2_dispatch(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                           const CUtensorMap& mv, int mode, bool bf16, dim3 grid, cudaStream_t s) {
-  return bf16 ? launch_cta2_typed<true>(p, mq, mk, mv, mode, grid, s)
-              : launch_cta2_typed<false>(p, mq, mk, mv, mode, grid, s);
+  return bf16 ? launch_cta2_typed<D, true>(p, mq, mk, mv, mode, grid, s)
+              : launch_cta2_typed<D, false>(p, mq, mk, mv, mode, grid, s);
 }
 
 }  // namespace attn
