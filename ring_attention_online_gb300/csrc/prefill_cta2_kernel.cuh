@@ -180,6 +180,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
       it.h = blockIdx.y;
       it.u_lo = w.z;
       it.u_hi = w.z + w.w;
+      if (p.causal && (((w.y + C::BM - 1) / C::BM) & 1)) {
+        // a causal sequence of an odd number of 128-row Q tiles: its first
+        // tile (a one-tile walk) goes without a partner rather than its last
+        // (the longest walk), so item t holds Q tiles 2t - 1 and 2t
+        const int t = (w.z - w.x) / (2 * C::BM);
+        it.u_lo = t == 0 ? w.x : w.x + (2 * t - 1) * C::BM;
+        it.u_hi = min(it.u_lo + (t == 0 ? 1 : 2) * C::BM, w.x + w.y);
+      }
       it.kv_lo = w.x;
       it.kv_hi = w.x + w.y;  // seq_offsets[seq_idx + 1]
       it.q_pos0 = 0;

@@ -129,10 +129,25 @@ __device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int k, int
   if constexpr (kMode == kModeJagged) {
     // a 256-row Q tile of one sequence (a failed check reads an empty item)
     const int4 w = check_index(k, *p.work_count, &g_prefill_status) ? p.work_items[k] : make_int4(0, 0, 0, 0);
-    const int a_hi = w.z + min(w.w, BM);
+    int lo = w.z, mid = w.z + min(w.w, BM), hi = w.z + w.w;
+    if (p.causal) {
+      // A causal sequence of an odd number m of 128-row Q tiles leaves one
+      // tile without a partner.  Its first tile (a one-tile walk) takes that
+      // place rather than its last (the longest walk): item t of the sequence
+      // holds Q tiles 2t - 1 and 2t, item 0 tile 0 alone.  The item count,
+      // ceil(m / 2), is the worklist's.
+      const int m = (w.y + BM - 1) / BM;
+      if (m & 1) {
+        const int t = (w.z - w.x) / (2 * BM);
+        const int seq_end = w.x + w.y;
+        lo = t == 0 ? w.x : w.x + (2 * t - 1) * BM;
+        mid = min(lo + BM, seq_end);
+        hi = t == 0 ? mid : min(lo + 2 * BM, seq_end);
+      }
+    }
     it.b = 0;
-    it.st0 = SubTile{h, w.z, a_hi};
-    it.st1 = SubTile{h, a_hi, w.z + w.w};
+    it.st0 = SubTile{h, lo, mid};
+    it.st1 = SubTile{h, mid, hi};
     it.kv_lo = w.x;
     it.kv_hi = w.x + w.y;  // seq_offsets[seq_idx + 1]
     it.q_pos0 = 0;
