@@ -43,12 +43,16 @@
 //               The copies of both CTAs complete on rank 0's barriers
 //               (cta_group::2 form), which rank 0 arms for the bytes of both,
 //               so one wait tells an issuer that both halves have landed.
-//   warp 1      TMEM owner; rank 0: S issuer, S(j) = Q.K_j^T for the pair.
-//   warp 10     rank 0: P.V issuer.  rank 1: idle.
+//   warp 1      TMEM owner; rank 0: S issuer, S(j) = Q.K_j^T for the pair,
+//               once K(j) has landed and both CTAs' softmax warps have read
+//               S(j-1) (one barrier: the K stage's).
+//   warp 10     rank 0: P.V issuer, once V(j) has landed and P(j) is written
+//               (one barrier: the V stage's).  rank 1: idle.
 //   warps 2..9  softmax of this CTA's 128 rows, two warps per row (a half of
 //               the tile's keys and of O's columns each, the pair of warps
 //               exchanging row maxima once per tile); their "S read" and "P
-//               written" signals go to rank 0's barriers (one arrival per warp).
+//               written" signals go to rank 0's K and V stage barriers (one
+//               arrival per warp).
 //               At the end of an item they leave each row's (m, l) in shared
 //               memory and go on to the next item.
 //   warps 11..14 epilogue of this CTA's 128 rows, one warp per TMEM lane
@@ -133,8 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
   __shared__ uint64_t bar_q, bar_qe, bar_fin, bar_exit;
   __shared__ uint64_t bar_o[2];  // PV(j) completes a phase of bar_o[j % 2] (both CTAs)
   __shared__ uint64_t bar_full[C::NST], bar_empty[C::NST];
-  __shared__ uint64_t bar_s[2], bar_p[2];
-  __shared__ uint64_t bar_sfree[2];  // the pair's softmax warps have read S(j) out of TMEM (j % 2)
+  __shared__ uint64_t bar_s[2];
   __shared__ uint32_t tmem_slot;
   __shared__ uint32_t abort_flag;
   __shared__ float xch_max[2][C::WPR][128];  // [tile parity][key part][row]
@@ -250,14 +253,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
     mbar_init(&bar_o[1], 1);
     mbar_init(&bar_fin, 2);  // one commit per MMA issuer, multicast to both CTAs
     mbar_init(&bar_exit, 1);
+    // a K stage's fill for tile j completes once its copies have landed and
+    // the pair's softmax warps have read S(j - 1) (the one S buffer is free);
+    // a V stage's fill for tile j once its copies have landed and the softmax
+    // warps have written P(j): one wait per tile for each MMA issuer
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_full[s], 1 + C::kSignals);
       mbar_init(&bar_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
-      mbar_init(&bar_sfree[i], C::kSignals);
-      mbar_init(&bar_p[i], C::kSignals);
       for (int q4 = 0; q4 < 4; ++q4) mbar_init(&bar_x[i][q4], 32 * C::WPR);
       mbar_init(&bar_ep_full[i], 32 * C::SM_WARPS);
       mbar_init(&bar_ep_empty[i], 32 * 4);
@@ -350,25 +355,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
         }
       }
       if (abort_flag) {
-        // copies may still be landing in this CTA's shared memory: wait for them
-        if (rank == 0) {
-          // rank 0's barriers see the copies of both CTAs (a fill that rank 1
-          // never issued leaves its phase open: that wait gives up, bounded)
-          if (q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
-          for (int ring = 0; ring < 2; ++ring) {
-            const int outstanding = filled[ring] < C::RING ? filled[ring] : C::RING;
-            for (int i = 0; i < outstanding; ++i) {
-              const int pos = filled[ring] - 1 - i;
-              pf_drain(&bar_full[ring * C::RING + pos % C::RING], (uint32_t)((pos / C::RING) & 1));
-            }
-          }
-        } else {
-          // rank 1's copies complete on rank 0's barriers, which it cannot poll:
-          // it waits far longer than a copy takes (rank 0 waits for it at the
-          // exit handshake, so its barriers outlive the copies)
-          const uint64_t t0 = global_timer_ns();
-          while (global_timer_ns() - t0 < C::kPeerCopyDrainNs) {
-          }
+        // copies may still be landing in this CTA's shared memory: wait for
+        // them.  A stage's phase also counts softmax signals that an aborted
+        // pipeline may never send, and rank 1's copies complete on rank 0's
+        // barriers, which it cannot poll, so both CTAs wait a fixed time far
+        // longer than a copy takes (the CTAs then meet at the exit handshake,
+        // so rank 0's barriers outlive rank 1's copies); rank 0 first drains
+        // its Q barrier, which counts copies only.
+        if (rank == 0 && q_loads > 0) pf_drain(&bar_q, (uint32_t)((q_loads - 1) & 1));
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < C::kPeerCopyDrainNs) {
         }
       }
     }
@@ -412,13 +408,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
           tc_fence_after_sync();
           ++q_used;
           for (int j = 0; ok && j < n; ++j, ++g) {
-            if (g >= 1) {
-              // the one S buffer is free once both CTAs' softmax warps have read S(j-1)
-              ok = pf_wait_outlined(&bar_sfree[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), &abort_flag, 11);
-              if (!ok) break;
-              tc_fence_after_sync();
-            }
             {
+              // K(j) has landed and the softmax warps of both CTAs have read
+              // S(j-1): the one S buffer is free
               const int tl = tile_base + j;
               ok = wait_tile(0, tl, 2);
               if (!ok) break;
@@ -448,9 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
           }
           ++o_items;
           for (int j = 0; ok && j < n; ++j, ++g) {
-            ok = pf_wait_outlined(&bar_p[g & 1], (uint32_t)((g >> 1) & 1), &abort_flag, 3);
-            if (!ok) break;
-            tc_fence_after_sync();  // P of both CTAs in TMEM
+            // V(j) has landed and P(j) of both CTAs is in TMEM (one barrier)
             const uint32_t p_tmem = tmem + C::P_COL + static_cast<uint32_t>((g & 1) * 64);
             const uint32_t acc0 = j > 0 ? 1u : 0u;  // the item's first PV starts O afresh
             {
@@ -492,15 +482,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
     const int row = wq * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;  // > 0
-    const uint32_t sfree_remote[2] = {mapa_shared(&bar_sfree[0], 0), mapa_shared(&bar_sfree[1], 0)};
-    const uint32_t p_remote[2] = {mapa_shared(&bar_p[0], 0), mapa_shared(&bar_p[1], 0)};
-    // one arrival per warp on rank 0's barrier: local there, remote from rank 1
-    auto signal = [&](uint64_t* local, uint32_t remote) {
+    // one arrival per warp on rank 0's barrier of a stage: local there,
+    // remote from rank 1
+    auto signal = [&](int stage) {
       if (rank == 0)
-        mbar_arrive(local);
+        mbar_arrive(&bar_full[stage]);
       else
-        mbar_arrive_remote(remote);
+        mbar_arrive_remote(mapa_shared(&bar_full[stage], 0));
     };
+    // the K stage of the first tile waits for no S read
+    __syncwarp();
+    if (lane == 0) signal(0);
     bool ok = true;
     int gj = 0;    // tiles so far, all items: the phases of the per-tile barriers
     int n_ep = 0;  // epilogues so far
@@ -532,7 +524,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
         // S(j) is in registers: the S issuer may overwrite the buffer with S(j+1)
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) signal(&bar_sfree[buf], sfree_remote[buf]);
+        if (lane == 0) signal((gj + 1) % C::RING);  // the K stage of tile gj + 1
 
         // mask the diagonal / tail tile (key kstart + i is visible iff i < lim)
         // and, under a sliding window, the tiles at its lower edge (iff i >= flo);
@@ -649,7 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) signal(&bar_p[buf], p_remote[buf]);
+        if (lane == 0) signal(C::RING + gj % C::RING);  // the V stage of tile gj
       }
       if (ok && n > 0) {
         // hand the row's state to the epilogue warps (one buffer per item
