@@ -79,17 +79,17 @@ struct Cta2Cfg {
   static constexpr int D = D_;
   static constexpr int BM = 128;                // query rows per CTA (256 per pair)
   static constexpr int BN = 128;                // keys per KV tile
-  static constexpr int SC = 128;                // columns of D per P.V MMA (a half of D)
-  static constexpr int NH = D / SC;             // halves of D
   static constexpr int KH = BN / 2;             // keys of a K tile each CTA holds
-  static constexpr int VH = SC / 2;             // columns of each half of D of V each CTA holds
+  static constexpr int VB = D / 128;            // 64-column blocks of V each CTA holds (its half of D)
   static constexpr int Q_BLOCK = 128 * 128;     // Q: 128 rows x 64 columns (128 B, swizzled)
   static constexpr int K_BLOCK = KH * 128;      // K half: 64 keys x 64 columns
   static constexpr int V_BLOCK = BN * 128;      // V: 128 keys x 64 columns
   static constexpr int Q_BYTES = BM * D * 2;    // 64 KB at head dim 256
-  // one stage per K or V tile: this CTA's 64 keys x 256 columns of K, or the
-  // tile's 128 keys x this CTA's 2 x 64 columns of V (one 64-column block per
-  // 128-column half of D).  One barrier per tile: each wait of an MMA issuer
+  // one stage per K or V tile: this CTA's 64 keys x D columns of K, or the
+  // tile's 128 keys x this CTA's D / 2 columns of V (rank r holds columns
+  // [r D / 2, (r + 1) D / 2), so one P.V MMA of N = D covers all of O: at head
+  // dim 256, 8 MMAs of 128 cycles per tile instead of 16 of 64, which halves
+  // what the issuing thread must keep up with).  One barrier per tile: each wait of an MMA issuer
   // costs the tensor pipe a bubble (the wait holds the issuing thread until its
   // MMAs drain), and with one wait per slab (two per tile) the kernel ran
   // 1428-1510 vs 1471-1558 TFLOP/s on dense causal B=8 H=32 S=4096.
@@ -122,7 +122,7 @@ struct Cta2Cfg {
   static constexpr uint32_t kEpiSignals = 2 * 4;       // "O free": every epilogue warp of the pair
   static_assert(WPR == 2 || WPR == 4, "softmax warps per row");
   static_assert(D == 128 || D == 256, "CTA-pair kernel: head dim 128 or 256");
-  static_assert(BN * VH * 2 * NH == STAGE_BYTES, "a K and a V stage are the same size");
+  static_assert(BN * 64 * VB * 2 == STAGE_BYTES, "a K and a V stage are the same size");
   static_assert(RING >= 2, "K(j+1) must be loadable while K(j) is read");
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES + 13 * 1024 <= 227 * 1024, "shared memory budget (static part < 13 KB)");
@@ -316,8 +316,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
             load(dst + blk * C::K_BLOCK, &mk, full0, blk * 64, hk, kstart + C::KH * (int)rank, bb, p.h_kv, p.S_kv);
         } else {
           // V: the tile's 128 keys, this CTA's 64 columns of each 128-column half
-          for (int hs = 0; hs < C::NH; ++hs)
-            load(dst + hs * C::V_BLOCK, &mv, full0, hs * C::SC + C::VH * (int)rank, hk, kstart, bb, p.h_kv, p.S_kv);
+          for (int vb = 0; vb < C::VB; ++vb)
+            load(dst + vb * C::V_BLOCK, &mv, full0, (int)rank * (D / 2) + 64 * vb, hk, kstart, bb, p.h_kv, p.S_kv);
         }
         ++fills;
         return true;
@@ -382,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
     // issuer on P(j) and on V(j).
     if (lane == 0 && rank == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(256, C::BN, kBf16, false);
-      constexpr uint32_t kIdescPV = idesc_f16_f32acc(256, C::SC, kBf16, true);
+      constexpr uint32_t kIdescPV = idesc_f16_f32acc(256, D, kBf16, true);
       const uint32_t skv = smem_u32(sKV);
       auto wait_tile = [&](int ring, int f, uint32_t site) -> bool {
         const int stage = ring * C::RING + f % C::RING;
@@ -448,12 +448,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
               ok = wait_tile(1, tl, 4);
               if (!ok) break;
               const int stage = C::RING + tl % C::RING;
-              for (int hs = 0; hs < C::NH; ++hs) {
-                const uint64_t vdesc = smem_desc_sw128(skv + stage * C::STAGE_BYTES + hs * C::V_BLOCK, 16384, 1024);
-                // 16 keys of V per MMA (16 rows of 128 bytes)
+              {
+                // this CTA's D / 2 columns of V: 64-column blocks 16 KB apart
+                const uint64_t vdesc = smem_desc_sw128(skv + stage * C::STAGE_BYTES, C::V_BLOCK, 1024);
+                // 16 keys of V per MMA (16 rows of 128 bytes in each block)
 #pragma unroll
                 for (int ks = 0; ks < C::BN / 16; ++ks)
-                  mma_ts_cta2(tmem + C::O_COL + hs * C::SC, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
+                  mma_ts_cta2(tmem + C::O_COL, p_tmem + ks * 8, desc_advance(vdesc, ks * 2048), kIdescPV,
                               ks > 0 ? 1u : acc0);
               }
               mma_commit_cta2(&bar_empty[stage], C::kBoth);
