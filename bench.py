@@ -284,7 +284,10 @@ def make_workload(name: str, device, batch=None, seq=None):
         # FLOP per byte), so HBM is its binding roofline; the tensor fraction is
         # reported beside it
         hbm_bytes = 4.0 * T * cfg["H"] * cfg["D"] * 2 + cfg["H"] * T * 4.0
-        w.update(step=step, units=flops / 1e12, unit="TFLOP/s", bound="hbm", launches=2, tensors=(q, k, v, o),
+        # the worklist builder is one kernel up to 1024 sequences, a count and a
+        # write kernel beyond; then the attention kernel
+        launches = (1 if len(lens) <= 1024 else 2) + 1
+        w.update(step=step, units=flops / 1e12, unit="TFLOP/s", bound="hbm", launches=launches, tensors=(q, k, v, o),
                  kernel_units=hbm_bytes / 1e9, tensor_units=flops / 1e12,
                  config={"workload": name, "num_seqs": cfg["num_seqs"], "total_tokens": T, "H": cfg["H"],
                          "D": cfg["D"], "len_range": [cfg["len_lo"], cfg["len_hi"]], "causal": True,

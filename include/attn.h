@@ -150,9 +150,10 @@ attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, 
  * contiguous).  The attention kernel then runs, for D = 64/128, one persistent
  * CTA per SM over (unit, head) pairs, a sequence's Q tiles back to back so its
  * K/V is re-read from L2 ("Grouping": successive Q items reuse the resident K/V
- * range); for D = 256 one CTA per (item, head).  No host synchronisation.
+ * range); for D = 256 one CTA pair per (item, head).  No host synchronisation.
  * Workspace: int item count, int unit count, 8 bytes pad, the int4 items, then
- * the int2 units {first item, item count}.
+ * the int2 units {first item, item count}; beyond 1024 sequences the builder
+ * also keeps a table of per-CTA counts after the units.
  *   q/k/v/o [total_tokens,H,D]; lse [H,total_tokens] fp32 or NULL;
  *   seq_offsets int32 [num_seqs+1], device memory, non-decreasing, from 0 to at
  *   most total_tokens, every length <= max_seqlen (violations are reported as

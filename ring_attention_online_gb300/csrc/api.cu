@@ -246,8 +246,10 @@ attn_status_t attn_merge(const float* m, const float* l, const float* o_unnorm, 
 size_t attn_jagged_workspace_bytes(int num_seqs, int total_tokens, int max_seqlen) {
   (void)max_seqlen;
   if (num_seqs < 0 || total_tokens < 0) return 0;
-  // counts, items (sized for 128-row Q tiles, the larger count), one unit per sequence
-  return 16 + 16 * jagged_max_items(num_seqs, total_tokens) + (((size_t)num_seqs * 8 + 15) & ~size_t(15));
+  // counts, items (sized for 128-row Q tiles, the larger count), one unit per
+  // sequence, then the builder's per-CTA table (beyond 1024 sequences)
+  return 16 + 16 * jagged_max_items(num_seqs, total_tokens) + (((size_t)num_seqs * 8 + 15) & ~size_t(15)) +
+         worklist_scratch_bytes(num_seqs);
 }
 
 attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -268,7 +270,11 @@ attn_status_t attn_jagged(const void* q, const void* k, const void* v, void* o, 
   if (paired(D) && (unsigned long long)num_seqs * H > 0x7fffffffULL) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* wl = static_cast<int*>(workspace);
-  st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, block, wl, (int)max_items, s);
+  // the builder's table follows this launch's units (its item count is at most
+  // the one the workspace size allows for)
+  int2* wl_scratch = reinterpret_cast<int2*>(reinterpret_cast<char*>(workspace) + 16 + 16 * max_items +
+                                             (((size_t)num_seqs * 8 + 15) & ~size_t(15)));
+  st = launch_worklist(seq_offsets, num_seqs, total_tokens, max_seqlen, block, wl, (int)max_items, wl_scratch, s);
   if (st != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
   PrefillParams p{};

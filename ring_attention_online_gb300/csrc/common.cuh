@@ -67,9 +67,12 @@ unsigned int prefill_d256_take_status(cudaStream_t s);
 attn_status_t launch_merge(const float* m, const float* l, const float* o, int C, int B, int S_q, int H, int D,
                            void* out, bool out_bf16, float* lse, cudaStream_t s);
 
-// Jagged worklist builder.
+// Jagged worklist builder; beyond 1024 sequences it uses `scratch`
+// (worklist_scratch_bytes(num_seqs) bytes of device memory, 8-byte aligned).
+constexpr int kWorklistBuckets = 64;  // tile-count buckets of the ordered worklist
 attn_status_t launch_worklist(const int32_t* seq_offsets, int num_seqs, int total_tokens, int max_seqlen,
-                              int block_m, int* count_and_items, int max_items, cudaStream_t s);
+                              int block_m, int* count_and_items, int max_items, int2* scratch, cudaStream_t s);
+size_t worklist_scratch_bytes(int num_seqs);
 unsigned int worklist_take_status(cudaStream_t s);
 attn_status_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t s);
 attn_status_t launch_selftest_bounds(int* buf, cudaStream_t s);

@@ -25,6 +25,13 @@
 //
 // Output buffer: int item count at word 0, int unit count at word 1, items
 // from byte 16 (max_items of them), then the units.
+//
+// Up to 1024 sequences one CTA builds the list.  Beyond that two kernels share
+// the work, so the cost no longer grows with the sequence count: a count kernel
+// (one thread per sequence) sums each CTA's items and units per tile-count
+// bucket into a small table (int2 per CTA and bucket, after the units), and a
+// write kernel gives each CTA its positions from that table and scans its own
+// sequences bucket by bucket.  Both produce the same list in the same order.
 #include "checked.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -45,7 +52,7 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
   const int lane = tid & 31;
   const int w = tid >> 5;
   const int nmax = (max_seqlen + block_m - 1) / block_m;
-  const bool bucketed = nmax <= 64;
+  const bool bucketed = nmax <= kWorklistBuckets;
   if (tid == 0) {
     s_base = 0;
     s_ubase = 0;
@@ -122,10 +129,164 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restric
   }
 }
 
+// Sequence b's tile count (0 for an invalid or empty sequence) and start.
+__device__ __forceinline__ int seq_tiles(const int32_t* __restrict__ offs, int b, int num_seqs, int total_tokens,
+                                         int max_seqlen, int block_m, int& begin, int& len, bool& bad) {
+  begin = 0;
+  len = 0;
+  bad = false;
+  if (b >= num_seqs) return 0;
+  begin = offs[b];
+  const int end = offs[b + 1];
+  len = end - begin;
+  if (begin < 0 || end > total_tokens || len < 0 || len > max_seqlen) {
+    bad = true;
+    len = 0;
+  }
+  return (len + block_m - 1) / block_m;
+}
+
+// Count kernel: CTA c sums, for each tile-count bucket, the items and units of
+// its sequences [1024 c, 1024 c + 1024) into counts[c * kWorklistBuckets + bucket].
+__global__ void __launch_bounds__(1024) worklist_count_kernel(const int32_t* __restrict__ offs, int num_seqs,
+                                                              int total_tokens, int max_seqlen, int block_m,
+                                                              int2* __restrict__ counts) {
+  __shared__ int s_items[kWorklistBuckets], s_units[kWorklistBuckets];
+  const int tid = threadIdx.x;
+  const int nmax = (max_seqlen + block_m - 1) / block_m;
+  const bool bucketed = nmax <= kWorklistBuckets;
+  if (tid < kWorklistBuckets) {
+    s_items[tid] = 0;
+    s_units[tid] = 0;
+  }
+  __syncthreads();
+  int begin, len;
+  bool bad;
+  const int nt = seq_tiles(offs, blockIdx.x * 1024 + tid, num_seqs, total_tokens, max_seqlen, block_m, begin, len, bad);
+  if (bad) atomicOr(&g_worklist_status, kStatusDeviceInput);
+  if (nt > 0) {
+    const int bucket = bucketed ? nmax - nt : 0;  // 0 .. nmax - 1: more tiles first
+    atomicAdd(&s_items[bucket], nt);
+    atomicAdd(&s_units[bucket], 1);
+  }
+  __syncthreads();
+  if (tid < kWorklistBuckets) counts[(size_t)blockIdx.x * kWorklistBuckets + tid] = make_int2(s_items[tid], s_units[tid]);
+}
+
+// Write kernel: CTA c writes the items and units of its sequences.  Bucket k's
+// items start after every item of the buckets before it (all CTAs) and those
+// of bucket k in CTAs before c; within the CTA a block scan in sequence order.
+__global__ void __launch_bounds__(1024) worklist_write_kernel(const int32_t* __restrict__ offs, int num_seqs,
+                                                              int total_tokens, int max_seqlen, int block_m,
+                                                              const int2* __restrict__ counts, int n_cta,
+                                                              int* __restrict__ out, int max_items) {
+  int4* items = reinterpret_cast<int4*>(out + 4);
+  int2* units = reinterpret_cast<int2*>(out + 4 + 4 * (size_t)max_items);
+  __shared__ long long warp_sums[32];
+  __shared__ int s_base[kWorklistBuckets], s_ubase[kWorklistBuckets], s_mine[kWorklistBuckets];
+  __shared__ long long s_col[kWorklistBuckets], s_ucol[kWorklistBuckets];  // bucket totals, all CTAs
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int w = tid >> 5;
+  const int nmax = (max_seqlen + block_m - 1) / block_m;
+  const bool bucketed = nmax <= kWorklistBuckets;
+  const int nb = bucketed ? nmax : 1;
+  // thread k < nb: bucket k's totals over all CTAs and over the CTAs before this one
+  long long before = 0, ubefore = 0;
+  if (tid < nb) {
+    long long col = 0, ucol = 0;
+    for (int c = 0; c < n_cta; ++c) {
+      const int2 e = counts[(size_t)c * kWorklistBuckets + tid];
+      col += e.x;
+      ucol += e.y;
+      if (c < (int)blockIdx.x) {
+        before += e.x;
+        ubefore += e.y;
+      }
+    }
+    s_col[tid] = col;
+    s_ucol[tid] = ucol;
+    s_mine[tid] = counts[(size_t)blockIdx.x * kWorklistBuckets + tid].y;
+  }
+  __syncthreads();
+  if (tid < nb) {
+    long long ib = before, ub = ubefore;
+    for (int k = 0; k < tid; ++k) {
+      ib += s_col[k];
+      ub += s_ucol[k];
+    }
+    s_base[tid] = (int)min(ib, (long long)0x7fffffff);
+    s_ubase[tid] = (int)min(ub, (long long)0x7fffffff);
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    long long total = 0, utotal = 0;
+    for (int k = 0; k < nb; ++k) {
+      total += s_col[k];
+      utotal += s_ucol[k];
+    }
+    out[0] = total < max_items ? (int)total : max_items;
+    out[1] = (int)utotal;  // consumers skip unit items at or beyond out[0]
+    if (total > max_items) atomicOr(&g_worklist_status, kStatusDeviceInput);
+  }
+  __syncthreads();
+  int begin, len;
+  bool bad;
+  const int nt = seq_tiles(offs, blockIdx.x * 1024 + tid, num_seqs, total_tokens, max_seqlen, block_m, begin, len, bad);
+  for (int k = 0; k < nb; ++k) {
+    if (s_mine[k] == 0) continue;  // the same for every thread of the CTA
+    const bool take = nt > 0 && (!bucketed || nt == nmax - k);
+    const int cnt = take ? nt : 0;
+    // block-wide exclusive scan of (tiles << 32) | units, both counts < 2^31
+    const long long v = ((long long)cnt << 32) | (take ? 1 : 0);
+    long long x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      long long y = warp_sums[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const long long z = __shfl_up_sync(0xffffffffu, y, d);
+        if (lane >= d) y += z;
+      }
+      warp_sums[lane] = y;
+    }
+    __syncthreads();
+    const long long ex = x - v + (w > 0 ? warp_sums[w - 1] : 0);
+    const int excl = (int)(ex >> 32), uexcl = (int)(ex & 0xffffffffLL);
+    if (take) {
+      for (int t = 0; t < nt; ++t) {
+        const long long pos = (long long)s_base[k] + excl + t;
+        if (pos < max_items) items[pos] = make_int4(begin, len, begin + t * block_m, min(block_m, len - t * block_m));
+      }
+      if (check_index((long long)s_ubase[k] + uexcl, num_seqs, &g_worklist_status))  // < num_seqs by construction
+        units[s_ubase[k] + uexcl] = make_int2(s_base[k] + excl, nt);
+    }
+    __syncthreads();  // warp_sums is reused by the next bucket's scan
+  }
+}
+
+size_t worklist_scratch_bytes(int num_seqs) {
+  const size_t n_cta = ((size_t)(num_seqs > 0 ? num_seqs : 0) + 1023) / 1024;
+  return n_cta * kWorklistBuckets * sizeof(int2);
+}
+
 attn_status_t launch_worklist(const int32_t* seq_offsets, int num_seqs, int total_tokens, int max_seqlen, int block_m,
-                              int* count_and_items, int max_items, cudaStream_t s) {
-  worklist_kernel<<<1, 1024, 0, s>>>(seq_offsets, num_seqs, total_tokens, max_seqlen, block_m, count_and_items,
-                                     max_items);
+                              int* count_and_items, int max_items, int2* scratch, cudaStream_t s) {
+  if (num_seqs <= 1024) {
+    worklist_kernel<<<1, 1024, 0, s>>>(seq_offsets, num_seqs, total_tokens, max_seqlen, block_m, count_and_items,
+                                       max_items);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  const int n_cta = (num_seqs + 1023) / 1024;
+  worklist_count_kernel<<<n_cta, 1024, 0, s>>>(seq_offsets, num_seqs, total_tokens, max_seqlen, block_m, scratch);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  worklist_write_kernel<<<n_cta, 1024, 0, s>>>(seq_offsets, num_seqs, total_tokens, max_seqlen, block_m, scratch, n_cta,
+                                               count_and_items, max_items);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

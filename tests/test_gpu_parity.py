@@ -391,9 +391,13 @@ def test_jagged_parity_and_worklist(causal, D, dtype):
     O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), causal)
     close_o(o, O, f"attn_jagged D={D} causal={causal} {dtype}")
     close_lse(lse, L)
-    # worklist: the same items as the oracle's flattened worklist, bit for bit.  Every
-    # head dim runs two 128-row sub-tiles per item (head dims 64/128 in one CTA, 256 on
-    # a CTA pair), so the Q tiles are 256 rows.
+    _check_worklist(ws, offs, lengths, causal)
+
+
+def _check_worklist(ws, offs, lengths, causal):
+    """The device worklist in `ws` against the oracle's flattened worklist, bit for bit.
+    Every head dim runs two 128-row sub-tiles per item (head dims 64/128 in one CTA,
+    256 on a CTA pair), so the Q tiles are 256 rows."""
     block_m = 256
     words = ws.view(torch.int32).cpu().numpy()
     count = int(words[0])
@@ -413,7 +417,7 @@ def test_jagged_parity_and_worklist(causal, D, dtype):
     n_units = int(words[1])
     max_items = (int(offs[-1]) + (len(offs) - 1) * (block_m - 1)) // block_m
     units = words[4 + 4 * max_items:4 + 4 * max_items + 2 * n_units].reshape(n_units, 2)
-    assert n_units == sum(1 for L in lengths if L > 0)
+    assert n_units == sum(1 for n in lengths if n > 0)
     assert units[0][0] == 0 and all(u[1] >= 1 for u in units)
     for u, u2 in zip(units, units[1:]):
         assert u2[0] == u[0] + u[1]
@@ -480,6 +484,82 @@ def test_output_base_16_bytes_past_32(D):
     close_o(o, O, "jagged, offset output")
     close_lse(lse, L)
     assert torch.all(buf[:8] == 0) and torch.all(buf[8 + q.numel():] == 0)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_jagged_odd_tile_counts(D):
+    """attn_jagged, causal: sequences of 1, 3, 5, 7 and 9 Q tiles of 128 rows (full and
+    ragged last tiles) next to even counts.  A causal sequence with an odd tile count is
+    cut into items {0}, {1, 2}, {3, 4}, ... (its first tile alone), the worklist's items
+    into 256-row tiles from the start; every row must still come out once and right."""
+    lengths = [128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 640, 700, 768, 896, 897, 1024, 1100, 1152,
+               1, 64, 130, 300, 520, 1000]
+    H = 2
+    q, k, v, o, lse, offs, _ = _jagged_case(lengths, H, D, seed=31 + D)
+    O, L = A.jagged_attention(q.cpu(), k.cpu(), v.cpu(), offs, 1 / math.sqrt(D), True)
+    close_o(o, O, f"attn_jagged odd tile counts D={D}")
+    close_lse(lse, L)
+
+
+def _sampled_jagged_parity(q, k, v, o, lse, offs, seqs, what):
+    """Sequences `seqs` of a packed jagged batch against the oracle, one by one."""
+    D = q.shape[-1]
+    for b in seqs:
+        lo, hi = int(offs[b]), int(offs[b + 1])
+        if hi == lo:
+            continue
+        sl = slice(lo, hi)
+        O, L = A.jagged_attention(q[sl].cpu(), k[sl].cpu(), v[sl].cpu(), np.array([0, hi - lo]), 1 / math.sqrt(D), True)
+        close_o(o[sl], O, f"{what}, sequence {b}")
+        close_lse(lse[:, sl], L)
+
+
+def test_jagged_many_sequences_worklist():
+    """More than 1024 sequences: the worklist is built by a count kernel and a write
+    kernel over several CTAs.  5000 sequences of the jagged workload's lengths (64 to
+    1024 tokens, so four tile-count buckets) with zero-length ones among them and
+    sequences on the builder's CTA boundaries: the list bit for bit against the oracle's,
+    and a seeded sample of sequences against the oracle."""
+    rng = np.random.default_rng(41)
+    lengths = rng.integers(64, 1025, 5000)
+    lengths[rng.choice(5000, 50, replace=False)] = 0
+    lengths[[0, 1023, 1024, 2047, 2048, 4999]] = [1024, 0, 513, 256, 64, 1000]
+    q, k, v, o, lse, offs, ws = _jagged_case(lengths, 1, 64, seed=43)
+    assert ra.attn_last_device_status() == 0
+    _check_worklist(ws, offs, lengths, True)
+    sample = sorted(set(rng.choice(5000, 60, replace=False).tolist()) | {0, 1023, 1024, 2047, 2048, 4999})
+    _sampled_jagged_parity(q, k, v, o, lse, offs, sample, "attn_jagged 5000 sequences")
+
+
+def test_jagged_many_sequences_unbucketed_order():
+    """More than 1024 sequences with a longest one of more than 64 tiles of 256 rows:
+    the worklist keeps sequence order (no tile-count buckets).  The list against the
+    oracle's, and a seeded sample of sequences (the long one among them, checked on its
+    first rows and sampled ones) against the oracle."""
+    rng = np.random.default_rng(42)
+    lengths = rng.integers(64, 1025, 1100)
+    lengths[700] = 16500
+    q, k, v, o, lse, offs, ws = _jagged_case(lengths, 1, 64, seed=44)
+    assert ra.attn_last_device_status() == 0
+    block_m = 256
+    words = ws.view(torch.int32).cpu().numpy()
+    count = int(words[0])
+    items = words[4:4 + 4 * count].reshape(count, 4)
+    ref = S.jagged_worklist(offs, block_m, 128, True)
+    assert count == len(ref)
+    assert sorted(map(tuple, items.tolist())) == sorted(
+        (it["ordered_begin"], it["range_len"], it["tile_start"], it["tile_extent"]) for it in ref)
+    # sequence order, each sequence's tiles first to last
+    assert all(a[0] <= b[0] for a, b in zip(items, items[1:]))
+    sample = sorted(set(rng.choice(1100, 40, replace=False).tolist()) - {700} | {0, 699, 701, 1099})
+    _sampled_jagged_parity(q, k, v, o, lse, offs, sample, "attn_jagged 1100 sequences")
+    # the long sequence: rows sampled across it, each against all the keys it sees
+    lo = int(offs[700])
+    rows = np.concatenate([np.arange(0, 300), np.sort(rng.choice(np.arange(300, 16500), 200, replace=False))])
+    seq = slice(lo, lo + 16500)
+    O, L = A.attention(q[None, seq].cpu(), k[None, seq].cpu(), v[None, seq].cpu(), 1 / 8, True, rows=rows)
+    close_o(o[seq][rows], O[0, rows], "attn_jagged 16500-token sequence, sampled rows")
+    close_lse(lse[:, seq][:, rows], L[0][:, rows])
 
 
 def test_jagged_random_lengths():
