@@ -230,7 +230,12 @@ def make_workload(name: str, device, batch=None, seq=None):
             pipelined over three streams: batch b+1's inputs copy in while batch b
             computes and batch b-1's outputs copy out (the link runs both ways at
             once).  Events keep each batch's buffers from being overwritten before
-            the previous step has used them."""
+            the previous step has used them.  Consecutive steps overlap too: a
+            step's inputs start copying in once the previous step's kernels are
+            enqueued, while its last outputs still copy out; the timed region
+            ends after the last step's outputs are on the host (`e2e_finish`).
+            Only the first step of a timed region holds its copies until the
+            region's start (`e2e_begin`): later steps' copies are behind it anyway."""
             B = cfg["B"]
             if not pipe:
                 pipe.update(h2d=torch.cuda.Stream(device), d2h=torch.cuda.Stream(device), started=False,
@@ -238,8 +243,10 @@ def make_workload(name: str, device, batch=None, seq=None):
                             ev_c=[torch.cuda.Event() for _ in range(B)],
                             ev_out=[torch.cuda.Event() for _ in range(B)])
             h2d, d2h = pipe["h2d"], pipe["d2h"]
-            pipe.setdefault("ev_start", torch.cuda.Event()).record(stream)
-            h2d.wait_event(pipe["ev_start"])  # the copies start inside the step
+            if pipe.get("hold", True):
+                pipe.setdefault("ev_start", torch.cuda.Event()).record(stream)
+                h2d.wait_event(pipe["ev_start"])  # the copies start inside the timed region
+                pipe["hold"] = False
             for b in range(B):
                 if pipe["started"]:
                     h2d.wait_event(pipe["ev_c"][b])  # the previous step has read batch b's inputs
@@ -263,8 +270,15 @@ def make_workload(name: str, device, batch=None, seq=None):
                         h[b].copy_(d[b], non_blocking=True)
                 pipe["ev_out"][b].record(d2h)
             pipe["started"] = True
-            stream.wait_event(pipe["ev_out"][B - 1])  # the step ends with its last output on the host
+
+        def e2e_begin():
+            pipe["hold"] = True
+
+        def e2e_finish(stream):
+            stream.wait_event(pipe["ev_out"][cfg["B"] - 1])  # the last step's last output is on the host
         w["e2e_step"] = e2e_step
+        w["e2e_begin"] = e2e_begin
+        w["e2e_finish"] = e2e_finish
         w["e2e_launches"] = cfg["B"]  # one prefill kernel per batch
     elif cfg["kind"] == "jagged":
         q, k, v, offs = syn.jagged_inputs(cfg, seed=0, device=device)
@@ -356,7 +370,10 @@ def host_link(device, nbytes: int = 256 << 20, reps: int = 5):
             "how": "pinned torch tensors, one cudaMemcpyAsync per copy, 256 MiB, best of 5"}
 
 
-def time_steps(step, K: int, W: int, device):
+def time_steps(step, K: int, W: int, device, finish=None, begin=None):
+    """Device time of K steps after W warm-up steps.  `begin()`, if given, runs right
+    after the start event is recorded; `finish(stream)` joins work the steps left on
+    other streams into `stream` before the end event."""
     import torch
     stream = torch.cuda.current_stream(device)
     for _ in range(W):
@@ -366,8 +383,12 @@ def time_steps(step, K: int, W: int, device):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
+    if begin is not None:
+        begin()
     for _ in range(K):
         step(stream)
+    if finish is not None:
+        finish(stream)
     end.record(stream)
     torch.cuda.synchronize(device)
     barrier()
@@ -522,7 +543,7 @@ def run_ours(args):
         stream = torch.cuda.current_stream(device)
         e2e_step = lambda s=None: w["e2e_step"](host_in, host_out, stream)  # noqa: E731
         K2 = max(3, K // 5)
-        ms_e2e = time_steps(e2e_step, K2, 2, device)
+        ms_e2e = time_steps(e2e_step, K2, 2, device, finish=w.get("e2e_finish"), begin=w.get("e2e_begin"))
         units_e2e, ms_e2e_max = aggregate(w["units"] * K2, ms_e2e, world, device)
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
