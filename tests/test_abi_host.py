@@ -76,7 +76,11 @@ def test_partial_merge_jagged_decode_validation(lib):
     assert lib.attn_merge(FAKE, FAKE, FAKE, 2, 1, 1, 1, 80, FAKE, 0, None, None) == 2
     assert lib.attn_merge(FAKE, FAKE, FAKE, 2, 0, 1, 1, 64, FAKE, 0, None, None) == 0
     ws = lib.attn_jagged_workspace_bytes(3, 1000, 600)
-    assert ws == 16 + 16 * ((1000 + 3 * 127) // 128) + 32  # counts, items, 3 units (padded to 16 bytes)
+    # counts, items, 3 units (padded to 16 bytes), then the worklist builder's table of
+    # 64 int2 per started block of 1024 sequences
+    assert ws == 16 + 16 * ((1000 + 3 * 127) // 128) + 32 + 512
+    assert lib.attn_jagged_workspace_bytes(3000, 10 ** 6, 1024) == \
+        16 + 16 * ((10 ** 6 + 3000 * 127) // 128) + 3000 * 8 + 3 * 512
     assert lib.attn_jagged(FAKE, FAKE, FAKE, FAKE, None, FAKE, 3, 1000, 600, 4, 128, 1, 0.1, 1, FAKE, ws - 1,
                            None) == 1
     assert lib.attn_jagged(FAKE, FAKE, FAKE, FAKE, None, None, 3, 1000, 600, 4, 128, 1, 0.1, 1, FAKE, ws,
