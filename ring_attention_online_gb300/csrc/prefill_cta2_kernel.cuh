@@ -20,10 +20,10 @@
 // tensor cycles, more than the shared memory delivers in that time (128 B per
 // cycle).  In a pair, one MMA instruction covers M = 256 rows: each CTA
 // supplies its own 128 rows of Q (and of P, from its TMEM) and half of the B
-// operand (64 keys of K, 64 columns of each 128-column V slab), and each CTA's
-// TMEM receives its own rows of S and O.  Per CTA and KV tile the shared
-// memory then moves 192 KB: the S MMAs read 96 KB, the P.V MMAs 32 KB, the
-// copies write 64 KB.
+// operand (64 keys of K; D / 2 columns of V, so one P.V MMA of N = D covers
+// all of O), and each CTA's TMEM receives its own rows of S and O.  Per CTA
+// and KV tile the shared memory then moves 192 KB: the S MMAs read 96 KB, the
+// P.V MMAs 32 KB, the copies write 64 KB.
 //
 // Work: a pair item is 256 query rows that walk one KV sequence: two
 // consecutive 128-row Q tiles of one (batch, head), the even CTA of the pair
@@ -34,7 +34,8 @@
 // persistent: cluster c takes units c, c + clusters, ..., a unit being two
 // items of one (batch, head or head pair) whose causal walks add up to the
 // same length (items x and n - 1 - x), the longer first.  A jagged cluster
-// takes one worklist item of 256 rows.
+// takes one worklist item of 256 rows (in a causal sequence with an odd number
+// of 128-row Q tiles, item t holds tiles 2t - 1 and 2t, item 0 tile 0 alone).
 //
 // CTA layout (480 threads; both CTAs of the pair run the same roles except
 // where noted):
@@ -61,11 +62,11 @@
 //               waits for it) and store O / l and the LSE.
 // Every MMA commit is multicast to both CTAs' barriers.  Every wait is bounded:
 // a timeout sets the library's device status, the CTA skips its remaining
-// work, waits for its copies in flight (rank 0 on its barriers; rank 1, whose
-// copies complete on rank 0's barriers, for a fixed time far longer than a
-// copy takes) and (rank 0) for its MMAs, and both CTAs meet at a bounded exit
-// handshake before freeing TMEM, so neither leaves while the other may still
-// signal it.
+// work, waits for its copies in flight (a fixed time far longer than a copy
+// takes: a stage's phase also counts softmax signals an aborted pipeline may
+// never send, and rank 1's copies complete on rank 0's barriers) and (rank 0)
+// for its MMAs, and both CTAs meet at a bounded exit handshake before freeing
+// TMEM, so neither leaves while the other may still signal it.
 #pragma once
 
 #include <math_constants.h>
