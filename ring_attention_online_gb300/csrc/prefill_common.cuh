@@ -69,6 +69,28 @@ __device__ __forceinline__ bool pf_wait_outlined(uint64_t* bar, uint32_t parity,
   return pf_wait_slow(a, parity, abort, site);
 }
 
+// Visible keys of a 32-key chunk whose first key is key c0 of its tile: bit i
+// is set iff flo <= c0 + i < lim.  The limits come clamped to [0, tile keys],
+// so a masked tile's scores are tested with 32-bit masks, not one pair of
+// 64-bit compares per score.
+__device__ __forceinline__ uint32_t chunk_mask(int c0, int flo, int lim) {
+  const int lo = min(max(flo - c0, 0), 32), hi = min(max(lim - c0, 0), 32);
+  const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+  const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+  return below_hi & ~below_lo;
+}
+
+// Scores of a 32-key chunk outside `mask` become -inf.
+__device__ __forceinline__ void apply_mask(uint32_t (&r)[32], uint32_t mask, uint32_t ninf) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = ((mask >> i) & 1u) ? r[i] : ninf;
+}
+
+// Clamp a key limit of a tile of `keys` keys to [0, keys].
+__device__ __forceinline__ int clamp_limit(long long v, int keys) {
+  return (int)(v < 0 ? 0 : (v > keys ? keys : v));
+}
+
 // Wait used only while tearing down after an abort: ignores the abort flag.
 __device__ __forceinline__ bool pf_drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);

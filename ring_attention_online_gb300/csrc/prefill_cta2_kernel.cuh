@@ -544,13 +544,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cta2Cfg<D>::MAX_THRE
             lim = lc < lim ? lc : lim;
             if (win) flo = lc - 1 - p.window;
           }
-          const long long lh = lim - kq * KW, fh = flo - kq * KW;  // limits within this part
+          // limits within this part, clamped to its keys
+          const int ilh = clamp_limit(lim - kq * KW, KW), ifh = clamp_limit(flo - kq * KW, KW);
           const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
 #pragma unroll
-          for (int cc = 0; cc < NKC; ++cc)
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (cc * 32 + k >= lh || cc * 32 + k < fh) r[cc][k] = ninf;
+          for (int cc = 0; cc < NKC; ++cc) apply_mask(r[cc], chunk_mask(cc * 32, ifh, ilh), ninf);
         }
         float mx8[8];
 #pragma unroll

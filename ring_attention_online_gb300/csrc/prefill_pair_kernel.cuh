@@ -533,6 +533,7 @@ __global__ void __launch_bounds__(352, 1)
               (win && (long long)it.kv_pos0 + kstart < (long long)it.q_pos0 + me_t.q_hi - 1 - p.window);
           long long lim = C::BN;  // key kstart + i is visible iff flo <= i < lim
           long long flo = 0;
+          int ilim = C::BN, iflo = 0;  // the same limits clamped to the tile
           if (need_mask) {
             lim = (long long)mend - kstart;
             if (p.causal) {
@@ -540,6 +541,8 @@ __global__ void __launch_bounds__(352, 1)
               lim = lc < lim ? lc : lim;
               if (win) flo = lc - 1 - p.window;
             }
+            ilim = clamp_limit(lim, C::BN);
+            iflo = clamp_limit(flo, C::BN);
           }
           // the first 64 columns are reduced while the second pair of loads is in flight
           uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -549,11 +552,18 @@ __global__ void __launch_bounds__(352, 1)
           tmem_ld_wait(r1);
           tmem_ld32(scol + 64, r2);
           tmem_ld32(scol + 96, r3);
+          // the persistent modes (many masked tiles) take 32-bit chunk masks;
+          // the other walks keep per-score compares, which allocate better there
           if (need_mask) {
+            if constexpr (kPersistent) {
+              apply_mask(r0, chunk_mask(0, iflo, ilim), ninf);
+              apply_mask(r1, chunk_mask(32, iflo, ilim), ninf);
+            } else {
   #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i >= lim || i < flo) r0[i] = ninf;
-              if (i + 32 >= lim || i + 32 < flo) r1[i] = ninf;
+              for (int i = 0; i < 32; ++i) {
+                if (i >= lim || i < flo) r0[i] = ninf;
+                if (i + 32 >= lim || i + 32 < flo) r1[i] = ninf;
+              }
             }
           }
           float mx8[8];
@@ -566,10 +576,15 @@ __global__ void __launch_bounds__(352, 1)
           tmem_ld_wait(r2);
           tmem_ld_wait(r3);
           if (need_mask) {
+            if constexpr (kPersistent) {
+              apply_mask(r2, chunk_mask(64, iflo, ilim), ninf);
+              apply_mask(r3, chunk_mask(96, iflo, ilim), ninf);
+            } else {
   #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i + 64 >= lim || i + 64 < flo) r2[i] = ninf;
-              if (i + 96 >= lim || i + 96 < flo) r3[i] = ninf;
+              for (int i = 0; i < 32; ++i) {
+                if (i + 64 >= lim || i + 64 < flo) r2[i] = ninf;
+                if (i + 96 >= lim || i + 96 < flo) r3[i] = ninf;
+              }
             }
           }
   #pragma unroll
