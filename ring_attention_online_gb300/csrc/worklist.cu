@@ -30,8 +30,15 @@
 // the work, so the cost no longer grows with the sequence count: a count kernel
 // (one thread per sequence) sums each CTA's items and units per tile-count
 // bucket into a small table (int2 per CTA and bucket, after the units), and a
-// write kernel gives each CTA its positions from that table and scans its own
-// sequences bucket by bucket.  Both produce the same list in the same order.
+// write kernel gives each CTA its positions from that table.  Both produce the
+// same list in the same order.
+//
+// All sequences of a bucket have the same tile count, so a sequence's first
+// item is its bucket's first position plus its rank among the bucket's earlier
+// sequences times that count: one pass over the sequences (ranks within a warp
+// by matching buckets, then a sum over the warps before it per bucket) places
+// every bucket at once.  Without buckets (sequence order, tile counts that
+// differ) a block-wide scan of the tile counts places them.
 #include "checked.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -39,95 +46,6 @@
 namespace attn {
 
 static __device__ unsigned int g_worklist_status;
-
-__global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restrict__ offs, int num_seqs,
-                                                        int total_tokens, int max_seqlen, int block_m,
-                                                        int* __restrict__ out, int max_items) {
-  int4* items = reinterpret_cast<int4*>(out + 4);
-  int2* units = reinterpret_cast<int2*>(out + 4 + 4 * (size_t)max_items);
-  __shared__ long long warp_sums[32];
-  __shared__ int s_base, s_ubase;
-  __shared__ int s_bad;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int w = tid >> 5;
-  const int nmax = (max_seqlen + block_m - 1) / block_m;
-  const bool bucketed = nmax <= kWorklistBuckets;
-  if (tid == 0) {
-    s_base = 0;
-    s_ubase = 0;
-    s_bad = 0;
-  }
-  __syncthreads();
-  const int passes = bucketed ? nmax : 1;
-  for (int pass = 0; pass < passes; ++pass) {
-    const int want = nmax - pass;  // tile count served by this pass (bucketed order)
-    for (int c0 = 0; c0 < num_seqs; c0 += 1024) {
-      const int b = c0 + tid;
-      int begin = 0, len = 0, nt = 0;
-      if (b < num_seqs) {
-        begin = offs[b];
-        const int end = offs[b + 1];
-        len = end - begin;
-        if (begin < 0 || end > total_tokens || len < 0 || len > max_seqlen) {
-          s_bad = 1;
-          len = 0;
-        }
-        nt = (len + block_m - 1) / block_m;
-      }
-      const bool take = bucketed ? (nt == want && nt > 0) : (nt > 0);
-      const int cnt = take ? nt : 0;
-      // block-wide exclusive scan of (tiles << 32) | units, both counts < 2^31
-      const long long v = ((long long)cnt << 32) | (take ? 1 : 0);
-      long long x = v;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, x, d);
-        if (lane >= d) x += y;
-      }
-      if (lane == 31) warp_sums[w] = x;
-      __syncthreads();
-      if (w == 0) {
-        long long y = warp_sums[lane];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const long long z = __shfl_up_sync(0xffffffffu, y, d);
-          if (lane >= d) y += z;
-        }
-        warp_sums[lane] = y;
-      }
-      __syncthreads();
-      const long long ex = x - v + (w > 0 ? warp_sums[w - 1] : 0);
-      const int excl = (int)(ex >> 32), uexcl = (int)(ex & 0xffffffffLL);
-      const int total = (int)(warp_sums[31] >> 32), utotal = (int)(warp_sums[31] & 0xffffffffLL);
-      const int base = s_base, ubase = s_ubase;
-      if (take) {
-        for (int t = 0; t < nt; ++t) {
-          const long long pos = (long long)base + excl + t;
-          if (pos < max_items) {
-            const int tile_start = begin + t * block_m;
-            const int extent = min(block_m, len - t * block_m);
-            items[pos] = make_int4(begin, len, tile_start, extent);
-          }
-        }
-        if (check_index((long long)ubase + uexcl, num_seqs, &g_worklist_status))  // < num_seqs by construction
-          units[ubase + uexcl] = make_int2(base + excl, nt);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        s_base = base + total;
-        s_ubase = ubase + utotal;
-      }
-      __syncthreads();
-    }
-  }
-  if (tid == 0) {
-    const int count = s_base < max_items ? s_base : max_items;
-    out[0] = count;
-    out[1] = s_ubase;  // consumers skip unit items at or beyond out[0]
-    if (s_bad || s_base > max_items) atomicOr(&g_worklist_status, kStatusDeviceInput);
-  }
-}
 
 // Sequence b's tile count (0 for an invalid or empty sequence) and start.
 __device__ __forceinline__ int seq_tiles(const int32_t* __restrict__ offs, int b, int num_seqs, int total_tokens,
@@ -144,6 +62,135 @@ __device__ __forceinline__ int seq_tiles(const int32_t* __restrict__ offs, int b
     len = 0;
   }
   return (len + block_m - 1) / block_m;
+}
+
+// One thread per sequence of a CTA's 1024 (nt its tile count, 0 if empty):
+// writes its items and its unit in bucketed order.  base[k] / ubase[k]: the
+// position of the CTA's first item / unit of bucket k (bucket k holds the
+// sequences of nmax - k tiles).  Every thread of the CTA calls it.
+__device__ void write_bucketed(int nt, int begin, int len, int nmax, int block_m, const int* base, const int* ubase,
+                               int (*s_wcnt)[kWorklistBuckets], int4* __restrict__ items, int max_items,
+                               int2* __restrict__ units, int num_seqs) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int w = tid >> 5;
+  const int nb = nmax;
+  for (int i = tid; i < 32 * kWorklistBuckets; i += blockDim.x) s_wcnt[i / kWorklistBuckets][i % kWorklistBuckets] = 0;
+  __syncthreads();
+  const int k = nt > 0 ? nmax - nt : -1;  // 0 .. nmax - 1: more tiles first
+  const unsigned peers = __match_any_sync(0xffffffffu, k);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));  // earlier lanes of the bucket
+  if (k >= 0 && rank_w == 0) s_wcnt[w][k] = __popc(peers);
+  __syncthreads();
+  // per bucket, the sequences of the warps before each warp
+  if (tid < nb) {
+    int run = 0;
+    for (int v = 0; v < 32; ++v) {
+      const int c = s_wcnt[v][tid];
+      s_wcnt[v][tid] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (k >= 0) {
+    const int r = s_wcnt[w][k] + rank_w;  // rank among the CTA's sequences of bucket k
+    const long long first = (long long)base[k] + (long long)r * nt;
+    for (int t = 0; t < nt; ++t) {
+      const long long pos = first + t;
+      if (pos < max_items) items[pos] = make_int4(begin, len, begin + t * block_m, min(block_m, len - t * block_m));
+    }
+    if (check_index((long long)ubase[k] + r, num_seqs, &g_worklist_status))  // < num_seqs by construction
+      units[ubase[k] + r] = make_int2((int)min(first, (long long)0x7fffffff), nt);
+  }
+}
+
+// One CTA, num_seqs <= 1024 (the launcher's choice): the tile-count buckets'
+// sizes in shared memory, then the one-pass write; without buckets, one
+// block-wide scan of the tile counts in sequence order.
+__global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restrict__ offs, int num_seqs,
+                                                        int total_tokens, int max_seqlen, int block_m,
+                                                        int* __restrict__ out, int max_items) {
+  int4* items = reinterpret_cast<int4*>(out + 4);
+  int2* units = reinterpret_cast<int2*>(out + 4 + 4 * (size_t)max_items);
+  __shared__ int s_wcnt[32][kWorklistBuckets];
+  __shared__ int s_items[kWorklistBuckets], s_units[kWorklistBuckets], s_base[kWorklistBuckets],
+      s_ubase[kWorklistBuckets];
+  __shared__ long long warp_sums[32];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int w = tid >> 5;
+  const int nmax = (max_seqlen + block_m - 1) / block_m;
+  const bool bucketed = nmax <= kWorklistBuckets;
+  if (tid < kWorklistBuckets) {
+    s_items[tid] = 0;
+    s_units[tid] = 0;
+  }
+  if (tid == 0) s_bad = num_seqs > (int)blockDim.x;  // never, by the launcher's choice
+  __syncthreads();
+  int begin, len;
+  bool bad;
+  const int nt = seq_tiles(offs, tid, num_seqs, total_tokens, max_seqlen, block_m, begin, len, bad);
+  if (bad) s_bad = 1;
+  if (bucketed) {
+    if (nt > 0) {
+      atomicAdd(&s_items[nmax - nt], nt);
+      atomicAdd(&s_units[nmax - nt], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      long long ib = 0, ub = 0;
+      for (int k = 0; k < nmax; ++k) {
+        s_base[k] = (int)min(ib, (long long)0x7fffffff);
+        s_ubase[k] = (int)ub;
+        ib += s_items[k];
+        ub += s_units[k];
+      }
+      out[0] = ib < max_items ? (int)ib : max_items;
+      out[1] = (int)ub;  // consumers skip unit items at or beyond out[0]
+      if (s_bad || ib > max_items) atomicOr(&g_worklist_status, kStatusDeviceInput);
+    }
+    __syncthreads();
+    write_bucketed(nt, begin, len, nmax, block_m, s_base, s_ubase, s_wcnt, items, max_items, units, num_seqs);
+    return;
+  }
+  // block-wide exclusive scan of (tiles << 32) | units, both counts < 2^31
+  const long long v = ((long long)nt << 32) | (nt > 0 ? 1 : 0);
+  long long x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    long long y = warp_sums[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const long long z = __shfl_up_sync(0xffffffffu, y, d);
+      if (lane >= d) y += z;
+    }
+    warp_sums[lane] = y;
+  }
+  __syncthreads();
+  const long long ex = x - v + (w > 0 ? warp_sums[w - 1] : 0);
+  const long long excl = ex >> 32;
+  const int uexcl = (int)(ex & 0xffffffffLL);
+  if (nt > 0) {
+    for (int t = 0; t < nt; ++t) {
+      const long long pos = excl + t;
+      if (pos < max_items) items[pos] = make_int4(begin, len, begin + t * block_m, min(block_m, len - t * block_m));
+    }
+    if (check_index((long long)uexcl, num_seqs, &g_worklist_status))  // < num_seqs by construction
+      units[uexcl] = make_int2((int)min(excl, (long long)0x7fffffff), nt);
+  }
+  if (tid == 0) {
+    const long long total = warp_sums[31] >> 32;
+    out[0] = total < max_items ? (int)total : max_items;
+    out[1] = (int)(warp_sums[31] & 0xffffffffLL);
+    if (s_bad || total > max_items) atomicOr(&g_worklist_status, kStatusDeviceInput);
+  }
 }
 
 // Count kernel: CTA c sums, for each tile-count bucket, the items and units of
@@ -175,7 +222,8 @@ __global__ void __launch_bounds__(1024) worklist_count_kernel(const int32_t* __r
 
 // Write kernel: CTA c writes the items and units of its sequences.  Bucket k's
 // items start after every item of the buckets before it (all CTAs) and those
-// of bucket k in CTAs before c; within the CTA a block scan in sequence order.
+// of bucket k in CTAs before c; within the CTA the one-pass bucketed write, or
+// without buckets a block scan in sequence order.
 __global__ void __launch_bounds__(1024) worklist_write_kernel(const int32_t* __restrict__ offs, int num_seqs,
                                                               int total_tokens, int max_seqlen, int block_m,
                                                               const int2* __restrict__ counts, int n_cta,
@@ -185,6 +233,7 @@ __global__ void __launch_bounds__(1024) worklist_write_kernel(const int32_t* __r
   __shared__ long long warp_sums[32];
   __shared__ int s_base[kWorklistBuckets], s_ubase[kWorklistBuckets], s_mine[kWorklistBuckets];
   __shared__ long long s_col[kWorklistBuckets], s_ucol[kWorklistBuckets];  // bucket totals, all CTAs
+  __shared__ int s_wcnt[32][kWorklistBuckets];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int w = tid >> 5;
@@ -232,41 +281,41 @@ __global__ void __launch_bounds__(1024) worklist_write_kernel(const int32_t* __r
   int begin, len;
   bool bad;
   const int nt = seq_tiles(offs, blockIdx.x * 1024 + tid, num_seqs, total_tokens, max_seqlen, block_m, begin, len, bad);
-  for (int k = 0; k < nb; ++k) {
-    if (s_mine[k] == 0) continue;  // the same for every thread of the CTA
-    const bool take = nt > 0 && (!bucketed || nt == nmax - k);
-    const int cnt = take ? nt : 0;
-    // block-wide exclusive scan of (tiles << 32) | units, both counts < 2^31
-    const long long v = ((long long)cnt << 32) | (take ? 1 : 0);
-    long long x = v;
+  if (bucketed) {
+    write_bucketed(nt, begin, len, nmax, block_m, s_base, s_ubase, s_wcnt, items, max_items, units, num_seqs);
+    return;
+  }
+  if (s_mine[0] == 0) return;  // no sequence with tiles here (the same for every thread of the CTA)
+  // block-wide exclusive scan of (tiles << 32) | units, both counts < 2^31
+  const long long v = ((long long)nt << 32) | (nt > 0 ? 1 : 0);
+  long long x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    long long y = warp_sums[lane];
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += y;
+      const long long z = __shfl_up_sync(0xffffffffu, y, d);
+      if (lane >= d) y += z;
     }
-    if (lane == 31) warp_sums[w] = x;
-    __syncthreads();
-    if (w == 0) {
-      long long y = warp_sums[lane];
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const long long z = __shfl_up_sync(0xffffffffu, y, d);
-        if (lane >= d) y += z;
-      }
-      warp_sums[lane] = y;
+    warp_sums[lane] = y;
+  }
+  __syncthreads();
+  const long long ex = x - v + (w > 0 ? warp_sums[w - 1] : 0);
+  const long long first = (long long)s_base[0] + (ex >> 32);
+  const int uexcl = (int)(ex & 0xffffffffLL);
+  if (nt > 0) {
+    for (int t = 0; t < nt; ++t) {
+      const long long pos = first + t;
+      if (pos < max_items) items[pos] = make_int4(begin, len, begin + t * block_m, min(block_m, len - t * block_m));
     }
-    __syncthreads();
-    const long long ex = x - v + (w > 0 ? warp_sums[w - 1] : 0);
-    const int excl = (int)(ex >> 32), uexcl = (int)(ex & 0xffffffffLL);
-    if (take) {
-      for (int t = 0; t < nt; ++t) {
-        const long long pos = (long long)s_base[k] + excl + t;
-        if (pos < max_items) items[pos] = make_int4(begin, len, begin + t * block_m, min(block_m, len - t * block_m));
-      }
-      if (check_index((long long)s_ubase[k] + uexcl, num_seqs, &g_worklist_status))  // < num_seqs by construction
-        units[s_ubase[k] + uexcl] = make_int2(s_base[k] + excl, nt);
-    }
-    __syncthreads();  // warp_sums is reused by the next bucket's scan
+    if (check_index((long long)s_ubase[0] + uexcl, num_seqs, &g_worklist_status))  // < num_seqs by construction
+      units[s_ubase[0] + uexcl] = make_int2((int)min(first, (long long)0x7fffffff), nt);
   }
 }
 

@@ -410,9 +410,12 @@ def _check_worklist(ws, offs, lengths, causal):
     # order: non-increasing Q-tile count per sequence, and each sequence's tiles first-to-last
     ntiles = [(r[1] + block_m - 1) // block_m for r in items]
     assert all(a >= b for a, b in zip(ntiles, ntiles[1:]))
+    # sequences of one tile count in index order (sequence starts ascend)
     for a, b in zip(items, items[1:]):
         if a[0] == b[0]:
             assert b[2] == a[2] + block_m
+        elif (a[1] + block_m - 1) // block_m == (b[1] + block_m - 1) // block_m:
+            assert a[0] < b[0]
     # units: one per non-empty sequence, covering its contiguous items in order
     n_units = int(words[1])
     max_items = (int(offs[-1]) + (len(offs) - 1) * (block_m - 1)) // block_m
