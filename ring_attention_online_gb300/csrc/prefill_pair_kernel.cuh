@@ -434,15 +434,18 @@ __global__ void __launch_bounds__(352, 1)
             ok = wait_slab(slab);
             if (!ok) break;
             const uint32_t stage_addr = skv + (slab % C::NST) * C::SLAB_BYTES;
-  #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              if (!act[x]) continue;
+            // one call per sub-tile, the sub-tile a compile-time constant (as a
+            // loop over both with early exits this issue code ran the long ring
+            // 4.8 % and the window 3.8 % slower)
+            auto serve = [&](auto x_c) {
+              constexpr int x = decltype(x_c)::value;
+              if (!ok || !act[x]) return;
               const bool last = x == 1 || !act[1];  // last reader of the stage
               if (s_role) {
                 if (groups[x] > 0) {
                   // the sub-tile's previous P.V has read its P
                   ok = pf_wait(&bar_o[x], (uint32_t)((groups[x] - 1) & 1), &abort_flag, 11);
-                  if (!ok) break;
+                  if (!ok) return;
                   tc_fence_after_sync();
                 }
                 const uint64_t kdesc = smem_desc_sw128(stage_addr, 16, 1024);
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(352, 1)
                 mma_commit(&bar_s[x]);
               } else {
                 ok = pf_wait(&bar_p[x], (uint32_t)(groups[x] & 1), &abort_flag, 3);
-                if (!ok) break;
+                if (!ok) return;
                 tc_fence_after_sync();
                 const uint64_t vdesc = smem_desc_sw128(stage_addr, 16384, 1024);
                 const uint32_t p_tmem = tmem + static_cast<uint32_t>(x * 128);
@@ -474,7 +477,9 @@ __global__ void __launch_bounds__(352, 1)
                 mma_commit(&bar_o[x]);
               }
               ++groups[x];
-            }
+            };
+            serve(std::integral_constant<int, 0>{});
+            serve(std::integral_constant<int, 1>{});
           }
           if (!ok) break;
           // the item's S MMAs, the last readers of its Q, release the Q buffer
