@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(352, 1)
             const uint32_t stage_addr = skv + (slab % C::NST) * C::SLAB_BYTES;
             // one call per sub-tile, the sub-tile a compile-time constant (as a
             // loop over both with early exits this issue code ran the long ring
-            // 4.8 % and the window 3.8 % slower)
+            // 4.4 % and the window 2.5 % slower)
             auto serve = [&](auto x_c) {
               constexpr int x = decltype(x_c)::value;
               if (!ok || !act[x]) return;
