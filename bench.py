@@ -35,6 +35,9 @@ if ROOT not in sys.path:
 
 METRIC = "causal-useful TFLOP/s (prefill) and HBM GB/s (decode) on 1 GB300 vs roofline"
 HEADLINE = "dense_causal_b8_h32_s4096_d256"
+# measured after the headline in the same run, each with its own roofline
+SECONDARY = ("jagged_causal_1152seq_h4_d128", "long_gqa_ring8_s32768_hq64_hkv8_d128",
+             "decode_splitkv_b8_hq64_hkv8_d128_kv1m", "window4096_gqa_s32768_hq64_hkv8_d128")
 # the pages' best pruned dense causal figure for this exact workload (Pallas backend,
 # hardware not stated): context, not a target
 PAGES_DENSE_CAUSAL_TFS = 225.8
@@ -568,8 +571,7 @@ def run_ours(args):
     # ---- secondary workloads (same rules: inputs in HBM, CUDA events, max over ranks)
     if not args.no_secondary and args.workload == HEADLINE and args.batch is None and args.seq is None:
         sec = []
-        for name in ("jagged_causal_1152seq_h4_d128", "long_gqa_ring8_s32768_hq64_hkv8_d128",
-                     "decode_splitkv_b8_hq64_hkv8_d128_kv1m", "window4096_gqa_s32768_hq64_hkv8_d128"):
+        for name in SECONDARY:
             w = make_workload(name, device)
             k2 = max(3, min(K, 20))
             ms2 = time_steps(w["step"], k2, W, device)

@@ -64,6 +64,18 @@ def test_reference_arm_nonzero_rank_is_silent():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
+def test_every_reported_workload_has_profiled_traffic():
+    """The roofline objects of the headline and of every secondary workload carry the DRAM
+    bytes per launch committed under profiles/ (traffic.json), not null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synthetic as syn
+    for name in (bench.HEADLINE,) + bench.SECONDARY:
+        assert name in syn.WORKLOADS
+        t = bench._profiled_traffic(name)
+        assert isinstance(t, int) and t > 0, name
+
+
 def test_roofline_objects():
     """Achieved = algorithmic units per launch / launch time; a workload bound by HBM
     (below the ridge point) reports its tensor fraction beside the binding roofline."""
